@@ -1,0 +1,174 @@
+/*
+ * Plain C oracle of the Generalized Neighborhood Attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY: called from tests/, __graft_entry__.smoke() and the
+ * CPU-baseline leg of bench.py, never from the product library.  It shares no
+ * code with the CUDA sources.
+ *
+ * What it computes (GNA page, "GNA稀疏注意力机制：视觉Transformer计算优化实践",
+ * §1.1 and §1.2; blockwise-free plain softmax as in the video tutorial page,
+ * "视频生成推理提速:稀疏注意力组合配置教程", §3.3):
+ *
+ *   per dimension:  leader(i) = min(floor(i/s)*s + off(s), L-1)
+ *                   start(i)  = clamp(leader(i) - floor(w/2), 0, L-w)
+ *   N(i) = { j : start_d(i) <= j_d < start_d(i) + w_d in every dimension d }
+ *   s_ij  = scale * <q_i, k_j>
+ *   lse_i = ln sum_{j in N(i)} exp(s_ij)
+ *   out_i = sum_{j in N(i)} exp(s_ij - lse_i) v_j
+ *
+ * off(s) = floor(s/2) (rule 0, group centre) or floor((s-1)/2) (rule 1).
+ * Inputs are float32 holding the exact values the GPU reads (bf16 values, or
+ * e4m3 codes); per-tensor scales are applied in double.  Everything is
+ * accumulated in double with the maximum subtracted first (two passes).
+ * Queries are split over POSIX threads.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+static int leader_of(int i, int L, int s, int rule)
+{
+    int off = (rule == 0) ? s / 2 : (s - 1) / 2;
+    int c = (i / s) * s + off;
+    return c < L - 1 ? c : L - 1;
+}
+
+static int start_of(int i, int L, int w, int s, int rule)
+{
+    int a = leader_of(i, L, s, rule) - w / 2;
+    if (a < 0) a = 0;
+    if (a > L - w) a = L - w;
+    return a;
+}
+
+/* Window start of every position 0..L-1 of one dimension (for pinning tests). */
+void gna_oracle_window_starts(int L, int w, int s, int rule, int *out)
+{
+    for (int i = 0; i < L; ++i) out[i] = start_of(i, L, w, s, rule);
+}
+
+typedef struct {
+    const float *q, *k, *v;
+    int B, heads, dims[3], win[3], str[3], d, rule;
+    double scale, sq, sk, sv;
+    const int64_t *sel;
+    int64_t begin, end;
+    double *out, *lse;
+    int status;
+} job_t;
+
+static void one_query(const job_t *J, int64_t row, int64_t flat, double *sbuf)
+{
+    const int T = J->dims[0], H = J->dims[1], W = J->dims[2];
+    const int64_t N = (int64_t)T * H * W;
+    const int d = J->d, heads = J->heads;
+    int64_t tok = flat % N;
+    int64_t bh = flat / N;
+    int h = (int)(bh % heads), b = (int)(bh / heads);
+    int x = (int)(tok % W), y = (int)((tok / W) % H), t = (int)(tok / ((int64_t)W * H));
+
+    int a0 = start_of(t, T, J->win[0], J->str[0], J->rule);
+    int a1 = start_of(y, H, J->win[1], J->str[1], J->rule);
+    int a2 = start_of(x, W, J->win[2], J->str[2], J->rule);
+
+    const float *qi = J->q + ((((int64_t)b * T + t) * H + y) * W + x) * heads * d + (int64_t)h * d;
+    double qs = J->scale * J->sq * J->sk;
+
+    /* pass 1: scores and their maximum */
+    int64_t n = 0;
+    double m = -INFINITY;
+    for (int kt = a0; kt < a0 + J->win[0]; ++kt)
+        for (int ky = a1; ky < a1 + J->win[1]; ++ky)
+            for (int kx = a2; kx < a2 + J->win[2]; ++kx) {
+                const float *kj = J->k + ((((int64_t)b * T + kt) * H + ky) * W + kx) * heads * d + (int64_t)h * d;
+                double acc = 0.0;
+                for (int c = 0; c < d; ++c) acc += (double)qi[c] * (double)kj[c];
+                double s = qs * acc;
+                sbuf[n++] = s;
+                if (s > m) m = s;
+            }
+
+    /* pass 2: exponentials, their sum, and the weighted sum of values */
+    double *o = J->out + row * d;
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    double z = 0.0;
+    n = 0;
+    for (int kt = a0; kt < a0 + J->win[0]; ++kt)
+        for (int ky = a1; ky < a1 + J->win[1]; ++ky)
+            for (int kx = a2; kx < a2 + J->win[2]; ++kx) {
+                const float *vj = J->v + ((((int64_t)b * T + kt) * H + ky) * W + kx) * heads * d + (int64_t)h * d;
+                double e = exp(sbuf[n++] - m);
+                z += e;
+                for (int c = 0; c < d; ++c) o[c] += e * (double)vj[c];
+            }
+    for (int c = 0; c < d; ++c) o[c] = o[c] / z * J->sv;
+    J->lse[row] = m + log(z);
+}
+
+static void *worker(void *arg)
+{
+    job_t *J = (job_t *)arg;
+    int64_t wsz = (int64_t)J->win[0] * J->win[1] * J->win[2];
+    double *sbuf = (double *)malloc(sizeof(double) * (size_t)wsz);
+    if (!sbuf) { J->status = -2; return NULL; }
+    for (int64_t r = J->begin; r < J->end; ++r) {
+        int64_t flat = J->sel ? J->sel[r] : r;
+        one_query(J, r, flat, sbuf);
+    }
+    free(sbuf);
+    return NULL;
+}
+
+/*
+ * q, k, v : float32 rasters [B, T, H, W, heads, d]
+ * sel     : flat query ids ((b*heads + h)*N + (t*H + y)*W + x), or NULL for all
+ *           B*heads*N queries in that order
+ * out     : double [nsel, d];  lse : double [nsel]
+ * Returns 0, -1 on invalid arguments, -2 on allocation failure.
+ */
+int gna_oracle_forward(const float *q, const float *k, const float *v,
+                       int B, int heads, const int dims[3], const int window[3],
+                       const int stride[3], int head_dim, int rule,
+                       double scale, double scale_q, double scale_k, double scale_v,
+                       const int64_t *sel, int64_t nsel,
+                       double *out, double *lse, int nthreads)
+{
+    if (B < 1 || heads < 1 || head_dim < 1 || (rule != 0 && rule != 1)) return -1;
+    for (int i = 0; i < 3; ++i)
+        if (!(1 <= stride[i] && stride[i] <= window[i] && window[i] <= dims[i])) return -1;
+    int64_t N = (int64_t)dims[0] * dims[1] * dims[2];
+    int64_t total = sel ? nsel : (int64_t)B * heads * N;
+    if (sel)
+        for (int64_t r = 0; r < nsel; ++r)
+            if (sel[r] < 0 || sel[r] >= (int64_t)B * heads * N) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > total) nthreads = total > 0 ? (int)total : 1;
+
+    job_t *jobs = (job_t *)calloc((size_t)nthreads, sizeof(job_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return -2; }
+    for (int i = 0; i < nthreads; ++i) {
+        job_t *J = &jobs[i];
+        J->q = q; J->k = k; J->v = v;
+        J->B = B; J->heads = heads; J->d = head_dim; J->rule = rule;
+        for (int c = 0; c < 3; ++c) { J->dims[c] = dims[c]; J->win[c] = window[c]; J->str[c] = stride[c]; }
+        J->scale = scale; J->sq = scale_q; J->sk = scale_k; J->sv = scale_v;
+        J->sel = sel; J->out = out; J->lse = lse;
+        J->begin = total * i / nthreads;
+        J->end = total * (i + 1) / nthreads;
+        J->status = 0;
+    }
+    int rc = 0;
+    if (nthreads == 1) {
+        worker(&jobs[0]);
+    } else {
+        for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, worker, &jobs[i]);
+        for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    }
+    for (int i = 0; i < nthreads; ++i) if (jobs[i].status) rc = jobs[i].status;
+    free(jobs);
+    free(th);
+    return rc;
+}
