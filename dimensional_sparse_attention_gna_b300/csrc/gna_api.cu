@@ -1,0 +1,376 @@
+// C ABI of libgna_b300.so (declared in include/gna.h): argument validation,
+// tile planning, TMA descriptor encoding and kernel launches.  Nothing here
+// allocates device memory; every call enqueues on the caller's stream.
+#include <cmath>
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include "../../include/gna.h"
+#include "gna_geometry.cuh"
+#include "gna_internal.h"
+
+namespace {
+
+thread_local std::string t_last_error;
+
+gna_status fail(gna_status s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+gna_status cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(GNA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int ilog2_exact(int v)
+{
+    if (v <= 0 || (v & (v - 1)) != 0) return -1;
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
+
+int elem_size(gna_dtype dt)
+{
+    switch (dt) {
+        case GNA_BF16: return 2;
+        case GNA_FP8_E4M3: return 1;
+        case GNA_F32: return 4;
+        default: return 0;
+    }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool dims_ok(const int dims[3])
+{
+    return dims != nullptr && dims[0] >= 1 && dims[1] >= 1 && dims[2] >= 1;
+}
+
+int64_t padded_volume(const int dims[3], const int tile[3])
+{
+    int64_t v = 1;
+    for (int d = 0; d < 3; ++d) v *= static_cast<int64_t>((dims[d] + tile[d] - 1) / tile[d]) * tile[d];
+    return v;
+}
+
+void default_tile(const int dims[3], int tile[3])
+{
+    // least padding first; among equals the shape nearest (1, 8, 16) for
+    // images (T = 1) and (2, 8, 8) for videos, in log2 distance
+    const int target[3] = {dims[0] == 1 ? 0 : 1, 3, dims[0] == 1 ? 4 : 3};
+    int64_t best_pad = -1;
+    int best_dist = 0, best_w = 0;
+    for (int lt = 0; lt <= 7; ++lt)
+        for (int lh = 0; lt + lh <= 7; ++lh) {
+            const int lw = 7 - lt - lh;
+            const int t[3] = {1 << lt, 1 << lh, 1 << lw};
+            const int64_t pad = padded_volume(dims, t);
+            const int dist = std::abs(lt - target[0]) + std::abs(lh - target[1]) + std::abs(lw - target[2]);
+            const bool better = best_pad < 0 || pad < best_pad ||
+                                (pad == best_pad && (dist < best_dist || (dist == best_dist && t[2] > best_w)));
+            if (better) {
+                best_pad = pad;
+                best_dist = dist;
+                best_w = t[2];
+                tile[0] = t[0];
+                tile[1] = t[1];
+                tile[2] = t[2];
+            }
+        }
+}
+
+gna_status check_tile(const int tile[3], int tlog[3])
+{
+    int prod = 1;
+    for (int d = 0; d < 3; ++d) {
+        tlog[d] = ilog2_exact(tile[d]);
+        if (tlog[d] < 0) return fail(GNA_ERR_INVALID_ARG, "tile[%d] = %d is not a positive power of two", d, tile[d]);
+        prod *= tile[d];
+    }
+    if (prod != gna::kTileElems) return fail(GNA_ERR_INVALID_ARG, "tile volume %d != %d", prod, gna::kTileElems);
+    return GNA_OK;
+}
+
+gna_status resolve_tile(const int dims[3], const int* tile_in, int tile[3], int tlog[3])
+{
+    if (tile_in == nullptr || (tile_in[0] == 0 && tile_in[1] == 0 && tile_in[2] == 0))
+        default_tile(dims, tile);
+    else
+        for (int d = 0; d < 3; ++d) tile[d] = tile_in[d];
+    return check_tile(tile, tlog);
+}
+
+gna_status check_geometry(const int dims[3], const int window[3], const int stride[3])
+{
+    if (!dims_ok(dims)) return fail(GNA_ERR_INVALID_ARG, "dims must be >= 1");
+    if (window == nullptr || stride == nullptr) return fail(GNA_ERR_INVALID_ARG, "window / stride is NULL");
+    for (int d = 0; d < 3; ++d) {
+        if (!(1 <= stride[d] && stride[d] <= window[d] && window[d] <= dims[d]))
+            return fail(GNA_ERR_INVALID_ARG,
+                        "dimension %d: need 1 <= stride (%d) <= window (%d) <= length (%d)", d, stride[d],
+                        window[d], dims[d]);
+    }
+    return GNA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D TMA view [rows, head_dim] of a tiled tensor, box = 128 rows x one
+// swizzle span (128 B, or the whole row when it is shorter).
+gna_status make_tile_map(CUtensorMap* map, const void* ptr, int64_t rows, int head_dim, int esize)
+{
+    auto enc = encode_fn();
+    if (enc == nullptr) return fail(GNA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    const int row_bytes = head_dim * esize;
+    const int span = row_bytes >= 128 ? 128 : row_bytes;
+    const CUtensorMapSwizzle sw =
+        span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(row_bytes)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(span / esize), static_cast<cuuint32_t>(gna::kTileElems)};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(map, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                     const_cast<void*>(ptr), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GNA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return GNA_OK;
+}
+
+gna_status permute_common(const void* src, void* dst, int B, int heads, const int dims[3], const int* tile_in,
+                          int head_dim, gna_dtype dtype, void* stream, bool to_tiled)
+{
+    if (src == nullptr || dst == nullptr) return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(src) || !aligned16(dst)) return fail(GNA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (B < 1 || heads < 1 || head_dim < 1) return fail(GNA_ERR_INVALID_ARG, "B, heads and head_dim must be >= 1");
+    if (!dims_ok(dims)) return fail(GNA_ERR_INVALID_ARG, "dims must be >= 1");
+    const int es = elem_size(dtype);
+    if (es == 0) return fail(GNA_ERR_INVALID_ARG, "unknown dtype %d", static_cast<int>(dtype));
+    if ((static_cast<int64_t>(head_dim) * es) % 4 != 0)
+        return fail(GNA_ERR_UNSUPPORTED, "head_dim * element size must be a multiple of 4 bytes");
+    int tile[3], tlog[3];
+    gna_status st = resolve_tile(dims, tile_in, tile, tlog);
+    if (st != GNA_OK) return st;
+    gna::PermuteGeom g{};
+    g.B = B;
+    g.heads = heads;
+    int64_t ntiles = 1;
+    for (int d = 0; d < 3; ++d) {
+        g.dims[d] = dims[d];
+        g.nt[d] = (dims[d] + tile[d] - 1) / tile[d];
+        g.tlog[d] = tlog[d];
+        ntiles *= g.nt[d];
+    }
+    const int64_t blocks = ntiles * B * heads;
+    if (blocks > INT32_MAX || static_cast<int64_t>(head_dim) * es > (1 << 20))
+        return fail(GNA_ERR_UNSUPPORTED, "tensor too large");
+    g.ntiles_total = static_cast<int>(ntiles);
+    g.row_bytes = head_dim * es;
+    cudaError_t e = gna::launch_permute(src, dst, g, to_tiled, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, to_tiled ? "permute launch" : "unpermute launch");
+    t_last_error.clear();
+    return GNA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gna_version(void) { return GNA_VERSION; }
+
+const char* gna_status_string(gna_status s)
+{
+    switch (s) {
+        case GNA_OK: return "GNA_OK";
+        case GNA_ERR_INVALID_ARG: return "GNA_ERR_INVALID_ARG";
+        case GNA_ERR_UNSUPPORTED: return "GNA_ERR_UNSUPPORTED";
+        case GNA_ERR_CUDA: return "GNA_ERR_CUDA";
+        case GNA_ERR_TIMEOUT: return "GNA_ERR_TIMEOUT";
+        default: return "GNA_ERR_UNKNOWN";
+    }
+}
+
+const char* gna_last_error(void) { return t_last_error.c_str(); }
+
+gna_status gna_tile_shape(const int dims[3], int tile[3])
+{
+    if (!dims_ok(dims) || tile == nullptr) return fail(GNA_ERR_INVALID_ARG, "dims must be >= 1");
+    default_tile(dims, tile);
+    return GNA_OK;
+}
+
+int64_t gna_tiled_elems(int B, int heads, const int dims[3], const int tile_in[3], int head_dim)
+{
+    if (B < 1 || heads < 1 || head_dim < 1 || !dims_ok(dims)) return -1;
+    int tile[3], tlog[3];
+    if (resolve_tile(dims, tile_in, tile, tlog) != GNA_OK) return -1;
+    int64_t n = static_cast<int64_t>(B) * heads * head_dim * gna::kTileElems;
+    for (int d = 0; d < 3; ++d) n *= (dims[d] + tile[d] - 1) / tile[d];
+    return n;
+}
+
+gna_status gna_permute(const void* src, void* dst, int B, int heads, const int dims[3], int head_dim,
+                       gna_dtype dtype, void* stream)
+{
+    return permute_common(src, dst, B, heads, dims, nullptr, head_dim, dtype, stream, true);
+}
+
+gna_status gna_unpermute(const void* src, void* dst, int B, int heads, const int dims[3], int head_dim,
+                         gna_dtype dtype, void* stream)
+{
+    return permute_common(src, dst, B, heads, dims, nullptr, head_dim, dtype, stream, false);
+}
+
+gna_status gna_permute_tiled(const void* src, void* dst, int B, int heads, const int dims[3], const int tile[3],
+                             int head_dim, gna_dtype dtype, void* stream)
+{
+    if (tile == nullptr) return fail(GNA_ERR_INVALID_ARG, "tile is NULL");
+    return permute_common(src, dst, B, heads, dims, tile, head_dim, dtype, stream, true);
+}
+
+gna_status gna_unpermute_tiled(const void* src, void* dst, int B, int heads, const int dims[3], const int tile[3],
+                               int head_dim, gna_dtype dtype, void* stream)
+{
+    if (tile == nullptr) return fail(GNA_ERR_INVALID_ARG, "tile is NULL");
+    return permute_common(src, dst, B, heads, dims, tile, head_dim, dtype, stream, false);
+}
+
+gna_status gna_tile_stats(const int dims[3], const int window[3], const int stride[3], const int tile_in[3],
+                          int leader_rule, int64_t* visited_kv_tiles, int64_t* partial_kv_tiles, int64_t* q_tiles)
+{
+    gna_status st = check_geometry(dims, window, stride);
+    if (st != GNA_OK) return st;
+    if (leader_rule != GNA_LEADER_CENTER && leader_rule != GNA_LEADER_LITERAL)
+        return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", leader_rule);
+    int tile[3], tlog[3];
+    st = resolve_tile(dims, tile_in, tile, tlog);
+    if (st != GNA_OK) return st;
+    // The visited box of a Q tile is a product of per-dimension ranges, so
+    // the totals over all Q tiles factor into per-dimension sums.
+    int64_t visited = 1, full = 1, nq = 1;
+    for (int d = 0; d < 3; ++d) {
+        const int nt = (dims[d] + tile[d] - 1) / tile[d];
+        const int off = gna::leader_offset(stride[d], leader_rule);
+        int64_t sum_cnt = 0, sum_full = 0;
+        for (int qt = 0; qt < nt; ++qt) {
+            const gna::DimRange r = gna::dim_range(qt, tile[d], dims[d], window[d], stride[d], off);
+            sum_cnt += r.k1 - r.k0 + 1;
+            for (int kt = r.k0; kt <= r.k1; ++kt) sum_full += gna::dim_tile_full(kt, tile[d], dims[d], window[d], r);
+        }
+        visited *= sum_cnt;
+        full *= sum_full;
+        nq *= nt;
+    }
+    if (visited_kv_tiles) *visited_kv_tiles = visited;
+    if (partial_kv_tiles) *partial_kv_tiles = visited - full;
+    if (q_tiles) *q_tiles = nq;
+    return GNA_OK;
+}
+
+gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
+                          const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
+                          const gna_options* opt, void* stream)
+{
+    if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
+        return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(lse))
+        return fail(GNA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (B < 1 || heads < 1) return fail(GNA_ERR_INVALID_ARG, "B and heads must be >= 1");
+    gna_status st = check_geometry(dims, window, stride);
+    if (st != GNA_OK) return st;
+    const int es = (dtype == GNA_BF16) ? 2 : (dtype == GNA_FP8_E4M3) ? 1 : 0;
+    if (es == 0) return fail(GNA_ERR_INVALID_ARG, "forward dtype must be GNA_BF16 or GNA_FP8_E4M3");
+    if (!((es == 2 && (head_dim == 32 || head_dim == 64 || head_dim == 128)) || (es == 1 && head_dim == 128)))
+        return fail(GNA_ERR_UNSUPPORTED, "head_dim %d is not supported for this dtype", head_dim);
+    const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
+    if (rule != GNA_LEADER_CENTER && rule != GNA_LEADER_LITERAL)
+        return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", rule);
+    if (opt && !(opt->scale >= 0.0f && std::isfinite(opt->scale)))
+        return fail(GNA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    if (opt && opt->descale && es != 1) return fail(GNA_ERR_INVALID_ARG, "descale is only used with GNA_FP8_E4M3");
+    if (opt && opt->descale && (reinterpret_cast<uintptr_t>(opt->descale) & 3u))
+        return fail(GNA_ERR_INVALID_ARG, "descale must be 4-byte aligned");
+
+    gna::FwdParams p{};
+    int tlog[3];
+    st = resolve_tile(dims, opt ? opt->tile : nullptr, p.tile, tlog);
+    if (st != GNA_OK) return st;
+    int64_t tiles_per_head = 1;
+    for (int d = 0; d < 3; ++d) {
+        p.dims[d] = dims[d];
+        p.win[d] = window[d];
+        p.str[d] = stride[d];
+        p.off[d] = gna::leader_offset(stride[d], rule);
+        p.tlog[d] = tlog[d];
+        p.nt[d] = (dims[d] + p.tile[d] - 1) / p.tile[d];
+        tiles_per_head *= p.nt[d];
+    }
+    const int64_t num_q_tiles = tiles_per_head * B * heads;
+    const int64_t rows = num_q_tiles * gna::kTileElems;
+    if (rows > INT32_MAX) return fail(GNA_ERR_UNSUPPORTED, "more than 2^31 tiled rows");
+    p.heads = heads;
+    p.tiles_per_head = static_cast<int>(tiles_per_head);
+    p.out = out;
+    p.lse = lse;
+    p.descale = (opt && es == 1) ? opt->descale : nullptr;
+    p.scale = (opt && opt->scale > 0.0f) ? opt->scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    p.fault_skip_kv = -1;
+    if (const char* f = std::getenv("GNA_TEST_SKIP_KV_LOAD")) p.fault_skip_kv = std::atoi(f);
+
+    if ((st = make_tile_map(&p.tmQ, q, rows, head_dim, es)) != GNA_OK) return st;
+    if ((st = make_tile_map(&p.tmK, k, rows, head_dim, es)) != GNA_OK) return st;
+    if ((st = make_tile_map(&p.tmV, v, rows, head_dim, es)) != GNA_OK) return st;
+
+    cudaError_t e = gna::launch_forward(p, head_dim, es, num_q_tiles, static_cast<cudaStream_t>(stream));
+    if (e == cudaErrorNotSupported) return fail(GNA_ERR_UNSUPPORTED, "no kernel for head_dim %d", head_dim);
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    t_last_error.clear();
+    return GNA_OK;
+}
+
+gna_status gna_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
+                       const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
+                       void* stream)
+{
+    return gna_forward_ex(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, nullptr, stream);
+}
+
+gna_status gna_get_status(void* stream)
+{
+    int status = 0;
+    cudaError_t e = gna::read_and_clear_status(&status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (status != 0) return fail(static_cast<gna_status>(status), "a kernel abandoned a pipeline wait");
+    return GNA_OK;
+}
+
+}  // extern "C"

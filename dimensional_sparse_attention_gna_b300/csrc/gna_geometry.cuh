@@ -1,0 +1,70 @@
+// Window geometry of Generalized Neighborhood Attention, shared by the host
+// launcher and the device kernels of this library.
+//
+// GNA page ("GNA稀疏注意力机制：视觉Transformer计算优化实践"), §1.1: a stride
+// moves each query's window from the sliding window (stride 1) to blocked
+// attention (stride = window); queries of one stride group share the window of
+// the group's leader.  Per dimension of length L, window w, stride s and leader
+// offset off:
+//     leader(i) = min(floor(i / s) * s + off, L - 1)
+//     start(i)  = clamp(leader(i) - floor(w / 2), 0, L - w)
+// Query i sees keys [start(i), start(i) + w) in every dimension.
+//
+// Because start() is non-decreasing in i, a box of queries [lo, hi] sees the
+// key range [start(lo), start(hi) + w - 1]; a KV tile lies inside every one of
+// those windows iff it starts at or after start(hi) and ends at or before
+// start(lo) + w - 1.  These two facts give the per-Q-tile KV-tile range (§1.1)
+// and the "mask only partial tiles" test (§2.1).
+#pragma once
+
+#include <cstdint>
+
+namespace gna {
+
+constexpr int kTileElems = 128;   // tokens per layout tile (one MMA M / N extent)
+
+__host__ __device__ __forceinline__ int window_start(int i, int L, int w, int s, int off)
+{
+    int c = (i / s) * s + off;
+    c = c < L - 1 ? c : L - 1;
+    int a = c - w / 2;
+    a = a > 0 ? a : 0;
+    return a < L - w ? a : L - w;
+}
+
+__host__ __device__ __forceinline__ int leader_offset(int s, int rule)
+{
+    return rule == 0 ? s / 2 : (s - 1) / 2;
+}
+
+// Range of KV tiles (inclusive) and the window-start extremes of the query
+// tile `qt` along one dimension.
+struct DimRange {
+    int k0, k1;        // first / last KV tile index visited
+    int smin, smax;    // window start of the first / last valid query
+};
+
+__host__ __device__ __forceinline__ DimRange dim_range(int qt, int t, int L, int w, int s, int off)
+{
+    int lo = qt * t;
+    int hi = lo + t - 1;
+    hi = hi < L - 1 ? hi : L - 1;
+    DimRange r;
+    r.smin = window_start(lo, L, w, s, off);
+    r.smax = window_start(hi, L, w, s, off);
+    r.k0 = r.smin / t;
+    r.k1 = (r.smax + w - 1) / t;
+    return r;
+}
+
+// True iff KV tile `kt` along this dimension needs no element mask for any
+// valid query of the Q tile: it lies inside every query's window and holds no
+// padding.
+__host__ __device__ __forceinline__ bool dim_tile_full(int kt, int t, int L, int w, const DimRange& r)
+{
+    int lo = kt * t;
+    int hi = lo + t - 1;
+    return lo >= r.smax && hi <= r.smin + w - 1 && hi < L;
+}
+
+}  // namespace gna

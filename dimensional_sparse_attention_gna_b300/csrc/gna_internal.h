@@ -1,0 +1,46 @@
+// Internal interface between the C-ABI shim (gna_api.cu) and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace gna {
+
+// Geometry of one permute / unpermute launch.
+struct PermuteGeom {
+    int64_t B;
+    int heads;
+    int dims[3];          // T, H, W
+    int nt[3];            // tiles per dimension
+    int tlog[3];          // log2 of the tile extent per dimension
+    int ntiles_total;     // nt[0] * nt[1] * nt[2]
+    int row_bytes;        // head_dim * element size (multiple of 4)
+};
+
+cudaError_t launch_permute(const void* src, void* dst, const PermuteGeom& g, bool to_tiled, cudaStream_t stream);
+
+// Parameters of one attention launch (passed by value as a __grid_constant__).
+struct FwdParams {
+    CUtensorMap tmQ, tmK, tmV;   // 2-D views [rows, head_dim] of the tiled q, k, v
+    void* out;                   // tiled bf16 [rows, head_dim]
+    float* lse;                  // tiled float [rows] or nullptr
+    const float* descale;        // e4m3 only: 3 device floats (q, k, v) or nullptr
+    int dims[3], win[3], str[3], off[3];
+    int tile[3], tlog[3], nt[3];
+    int heads;
+    int tiles_per_head;          // nt[0] * nt[1] * nt[2]
+    float scale;                 // softmax scale
+    int fault_skip_kv;           // test hook: >= 0 makes the producer skip that KV load
+};
+
+// Launches the fused forward kernel for (head_dim, element size) on `stream`
+// over `num_q_tiles` CTAs.  Returns cudaErrorNotSupported for a head_dim /
+// dtype pair without a kernel.
+cudaError_t launch_forward(const FwdParams& p, int head_dim, int elem_size, int64_t num_q_tiles,
+                           cudaStream_t stream);
+
+// Device status word: read-and-clear.
+cudaError_t read_and_clear_status(int* status, cudaStream_t stream);
+
+}  // namespace gna

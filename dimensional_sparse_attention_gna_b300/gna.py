@@ -1,0 +1,228 @@
+"""Thin ctypes binding of ``libgna_b300.so`` (C ABI in ``include/gna.h``).
+
+Argument marshalling only: every function forwards device pointers, sizes and
+the current CUDA stream to the C entry point of the same name and turns a
+non-zero status into :class:`GNAError`.  All computation happens in the
+library's CUDA kernels; there is no fallback.  PyTorch only provides device
+memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+GNA_OK = 0
+GNA_ERR_INVALID_ARG = 1
+GNA_ERR_UNSUPPORTED = 2
+GNA_ERR_CUDA = 3
+GNA_ERR_TIMEOUT = 4
+
+GNA_BF16 = 0
+GNA_FP8_E4M3 = 1
+GNA_F32 = 2
+
+GNA_LEADER_CENTER = 0
+GNA_LEADER_LITERAL = 1
+
+TILE_ELEMS = 128
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgna_b300.so")
+
+_DTYPE_CODES = {torch.bfloat16: GNA_BF16, torch.float8_e4m3fn: GNA_FP8_E4M3, torch.float32: GNA_F32}
+
+_I3 = ctypes.c_int * 3
+_P = ctypes.c_void_p
+_INT = ctypes.c_int
+
+
+class GNAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_status_name(status)}: {message}")
+        self.status = status
+
+
+def _status_name(s: int) -> str:
+    return {0: "GNA_OK", 1: "GNA_ERR_INVALID_ARG", 2: "GNA_ERR_UNSUPPORTED", 3: "GNA_ERR_CUDA",
+            4: "GNA_ERR_TIMEOUT"}.get(s, f"status {s}")
+
+
+class GNAOptions(ctypes.Structure):
+    _fields_ = [("tile", ctypes.c_int * 3), ("leader_rule", ctypes.c_int), ("scale", ctypes.c_float),
+                ("descale", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library.  Raises if it has not been built: there is no other path."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m dimensional_sparse_attention_gna_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        st = ctypes.c_int
+        i64 = ctypes.c_int64
+        L.gna_version.restype = ctypes.c_int
+        L.gna_status_string.restype = ctypes.c_char_p
+        L.gna_status_string.argtypes = [st]
+        L.gna_last_error.restype = ctypes.c_char_p
+        L.gna_tile_shape.restype = st
+        L.gna_tile_shape.argtypes = [_I3, _I3]
+        L.gna_tiled_elems.restype = i64
+        L.gna_tiled_elems.argtypes = [_INT, _INT, _I3, _P, _INT]
+        for name in ("gna_permute", "gna_unpermute"):
+            f = getattr(L, name)
+            f.restype = st
+            f.argtypes = [_P, _P, _INT, _INT, _I3, _INT, _INT, _P]
+        for name in ("gna_permute_tiled", "gna_unpermute_tiled"):
+            f = getattr(L, name)
+            f.restype = st
+            f.argtypes = [_P, _P, _INT, _INT, _I3, _I3, _INT, _INT, _P]
+        L.gna_forward.restype = st
+        L.gna_forward.argtypes = [_P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _INT, _P]
+        L.gna_forward_ex.restype = st
+        L.gna_forward_ex.argtypes = [_P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _INT,
+                                     ctypes.POINTER(GNAOptions), _P]
+        L.gna_tile_stats.restype = st
+        L.gna_tile_stats.argtypes = [_I3, _I3, _I3, _P, _INT, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                     ctypes.POINTER(i64)]
+        L.gna_get_status.restype = st
+        L.gna_get_status.argtypes = [_P]
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != GNA_OK:
+        raise GNAError(status, lib().gna_last_error().decode())
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def dtype_code(dtype: torch.dtype) -> int:
+    try:
+        return _DTYPE_CODES[dtype]
+    except KeyError:
+        raise ValueError(f"unsupported dtype {dtype}") from None
+
+
+def gna_version() -> int:
+    return lib().gna_version()
+
+
+def gna_tile_shape(dims) -> tuple[int, int, int]:
+    out = _I3()
+    _check(lib().gna_tile_shape(_I3(*dims), out))
+    return tuple(out)
+
+
+def gna_tiled_elems(B: int, heads: int, dims, head_dim: int, tile=None) -> int:
+    t = None if tile is None else ctypes.cast(_I3(*tile), _P)
+    n = lib().gna_tiled_elems(B, heads, _I3(*dims), t, head_dim)
+    if n < 0:
+        raise GNAError(GNA_ERR_INVALID_ARG, "invalid layout arguments")
+    return n
+
+
+def tiled_shape(B: int, heads: int, dims, head_dim: int, tile=None) -> tuple[int, ...]:
+    """Shape ``[B, heads, tiles, 128, head_dim]`` of a tiled tensor."""
+    n = gna_tiled_elems(B, heads, dims, head_dim, tile)
+    return (B, heads, n // (B * heads * TILE_ELEMS * head_dim), TILE_ELEMS, head_dim)
+
+
+def gna_permute(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims, head_dim: int,
+                tile=None, stream=None):
+    """Raster ``[B, T, H, W, heads, d]`` -> tiled ``[B, heads, tiles, 128, d]`` (zero padding)."""
+    code = dtype_code(src.dtype)
+    if dst.dtype != src.dtype:
+        raise ValueError("src and dst dtypes differ")
+    if tile is None:
+        st = lib().gna_permute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+    else:
+        st = lib().gna_permute_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
+                                     _stream_ptr(stream))
+    _check(st)
+
+
+def gna_unpermute(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims, head_dim: int,
+                  tile=None, stream=None):
+    """Tiled ``[B, heads, tiles, 128, d]`` -> raster ``[B, T, H, W, heads, d]``."""
+    code = dtype_code(src.dtype)
+    if dst.dtype != src.dtype:
+        raise ValueError("src and dst dtypes differ")
+    if tile is None:
+        st = lib().gna_unpermute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+    else:
+        st = lib().gna_unpermute_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
+                                       _stream_ptr(stream))
+    _check(st)
+
+
+def gna_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None,
+                B: int, heads: int, dims, window, stride, head_dim: int, *, tile=None,
+                leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, descale: torch.Tensor | None = None,
+                stream=None):
+    """GNA forward on tiled tensors (see ``include/gna.h``).
+
+    ``q, k, v``: bf16 or float8_e4m3fn, tiled; ``out``: bf16 tiled; ``lse``:
+    float32 ``[B, heads, tiles, 128]`` or None; ``descale``: float32 device
+    tensor of 3 values (e4m3 only) or None.
+    """
+    code = dtype_code(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if out.dtype != torch.bfloat16:
+        raise ValueError("out must be bfloat16")
+    if lse is not None and lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    plain = tile is None and leader_rule == GNA_LEADER_CENTER and scale == 0.0 and descale is None
+    if plain:
+        st = lib().gna_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+                               _I3(*window), _I3(*stride), head_dim, code, _stream_ptr(stream))
+    else:
+        opt = GNAOptions()
+        opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+        opt.leader_rule = leader_rule
+        opt.scale = scale
+        if descale is not None:
+            if descale.dtype != torch.float32 or descale.numel() != 3:
+                raise ValueError("descale must be 3 float32 values")
+            opt.descale = _ptr(descale)
+        st = lib().gna_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+                                  _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
+                                  _stream_ptr(stream))
+    _check(st)
+
+
+def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADER_CENTER):
+    """(visited KV tiles, KV tiles needing the element mask, Q tiles) of one (b, head) plane."""
+    v, p_, q = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    t = None if tile is None else ctypes.cast(_I3(*tile), _P)
+    _check(lib().gna_tile_stats(_I3(*dims), _I3(*window), _I3(*stride), t, leader_rule,
+                                ctypes.byref(v), ctypes.byref(p_), ctypes.byref(q)))
+    return v.value, p_.value, q.value
+
+
+def gna_get_status(stream=None):
+    """Synchronise the stream and raise if a kernel abandoned a pipeline wait."""
+    _check(lib().gna_get_status(_stream_ptr(stream)))

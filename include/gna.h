@@ -1,0 +1,177 @@
+/*
+ * gna.h -- C ABI of the B300 (sm_103a) Generalized Neighborhood Attention
+ * forward library (libgna_b300.so).
+ *
+ * What the library computes
+ * -------------------------
+ * GNA page ("GNA稀疏注意力机制：视觉Transformer计算优化实践"), §1.1: every
+ * query attends only to a window of keys around it on the 2-D / 3-D token
+ * grid; a per-dimension stride moves that window in jumps, from the sliding
+ * window of neighborhood attention (stride 1) to blocked attention (stride =
+ * window).  Written out, for a grid (T, H, W), window (wT, wH, wW) and stride
+ * (sT, sH, sW), per dimension of length L with window w and stride s:
+ *
+ *     leader(i) = min(floor(i / s) * s + off(s), L - 1)
+ *     start(i)  = clamp(leader(i) - floor(w / 2), 0, L - w)
+ *
+ * with off(s) = floor(s / 2) (GNA_LEADER_CENTER, the default: queries of a
+ * stride group share the window of the group's centre, so stride = window on a
+ * divisible grid is exactly blocked attention) or floor((s - 1) / 2)
+ * (GNA_LEADER_LITERAL; identical for odd strides).  Query i attends to the
+ * keys j with start_d(i) <= j_d < start_d(i) + w_d in every dimension, i.e.
+ * exactly wT*wH*wW keys (§1.2: O(n k) work), with
+ *
+ *     lse_i = ln sum_j exp(scale * <q_i, k_j>),
+ *     out_i = sum_j exp(scale * <q_i, k_j> - lse_i) v_j,   scale = 1/sqrt(d).
+ *
+ * Layouts
+ * -------
+ * raster : [B, T, H, W, heads, d]   (a 2-D image grid is T = 1)
+ * tiled  : [B, heads, nT, nH, nW, tT*tH*tW, d],  n_ = ceil(L_ / t_)
+ *          Inside a tile the element index is (it*tH + iy)*tW + ix.  Grid
+ *          positions past the end of a dimension (padding of the last tile)
+ *          are zero.  The tile (tT, tH, tW) has 128 elements, each a power of
+ *          two (GNA page §1.1: Q and KV are split into fixed-size
+ *          multi-dimensional tiles; §2.2: tokens are permuted into this order
+ *          before attention and back after it).
+ * gna_forward reads and writes the tiled layout; gna_permute / gna_unpermute
+ * convert.  lse is tiled like a d = 1 float tensor: [B, heads, tiles, 128],
+ * and gna_unpermute(head_dim = 1, GNA_F32) turns it into raster
+ * [B, T, H, W, heads].
+ *
+ * Conventions
+ * -----------
+ * * Every pointer is CUDA device memory owned by the caller (global memory on
+ *   the current device) and must be 16-byte aligned.  The library allocates
+ *   nothing per call.
+ * * `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Calls enqueue work and return GNA_OK without synchronising.
+ * * Argument errors are detected on the host before anything is enqueued and
+ *   return GNA_ERR_INVALID_ARG / GNA_ERR_UNSUPPORTED; nothing is launched.
+ *   Launch failures return GNA_ERR_CUDA.  gna_last_error() gives a message.
+ * * A kernel that gives up waiting on an internal pipeline barrier (a bound of
+ *   about two seconds) records GNA_ERR_TIMEOUT in a device status word and
+ *   exits cleanly; gna_get_status() reports it.
+ * * No C++ exception crosses this boundary.  Functions are thread-safe.
+ */
+#ifndef GNA_B300_H
+#define GNA_B300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GNA_VERSION 1
+
+typedef enum {
+    GNA_OK = 0,
+    GNA_ERR_INVALID_ARG = 1,  /* bad size, geometry, pointer or alignment */
+    GNA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim 96) */
+    GNA_ERR_CUDA = 3,         /* a CUDA runtime / driver call failed */
+    GNA_ERR_TIMEOUT = 4       /* a kernel abandoned a pipeline wait (device status) */
+} gna_status;
+
+typedef enum {
+    GNA_BF16 = 0,      /* bfloat16 */
+    GNA_FP8_E4M3 = 1,  /* float8 e4m3 ("fn": finite, max 448) */
+    GNA_F32 = 2        /* float32: permute / unpermute only (lse) */
+} gna_dtype;
+
+typedef enum {
+    GNA_LEADER_CENTER = 0,   /* off(s) = floor(s/2)      (default) */
+    GNA_LEADER_LITERAL = 1   /* off(s) = floor((s-1)/2) */
+} gna_leader_rule;
+
+/* Options of gna_forward_ex.  Zero-initialise for the defaults. */
+typedef struct {
+    int tile[3];          /* layout tile; {0,0,0} = gna_tile_shape(dims)               */
+    int leader_rule;      /* gna_leader_rule                                            */
+    float scale;          /* softmax scale; 0 = 1/sqrt(head_dim)                        */
+    const float* descale; /* GNA_FP8_E4M3 only: device pointer to 3 floats, the
+                             per-tensor dequantisation scales of q, k, v (value =
+                             code * descale); NULL = 1, 1, 1                           */
+} gna_options;
+
+/* ------------------------------------------------------------ layout ---- */
+
+/* Default tile of the tiled layout for a grid: 128 elements, powers of two,
+ * least zero padding first, then the preferred shapes (2,8,8) for 3-D grids
+ * and (1,8,16) for 2-D grids.  dims[0] = T (1 for images).
+ * Returns GNA_ERR_INVALID_ARG for non-positive dims. */
+gna_status gna_tile_shape(const int dims[3], int tile[3]);
+
+/* Number of elements of one tiled tensor: B*heads*nT*nH*nW*128*head_dim
+ * (returns -1 on invalid arguments; tile NULL = default tile). */
+int64_t gna_tiled_elems(int B, int heads, const int dims[3], const int tile[3], int head_dim);
+
+/* Raster -> tiled (zero padding) and tiled -> raster (padding dropped).
+ * src and dst must not overlap.  Any head_dim >= 1 with head_dim * element
+ * size a multiple of 4 bytes; dtype GNA_BF16, GNA_FP8_E4M3 or GNA_F32.
+ * The *_tiled variants take an explicit tile (128 elements, powers of two).
+ * GNA page §2.2 (memory operations: token permutation before and after the
+ * model, as a dedicated copy kernel). */
+gna_status gna_permute(const void* src, void* dst, int B, int heads, const int dims[3],
+                       int head_dim, gna_dtype dtype, void* stream);
+gna_status gna_unpermute(const void* src, void* dst, int B, int heads, const int dims[3],
+                         int head_dim, gna_dtype dtype, void* stream);
+gna_status gna_permute_tiled(const void* src, void* dst, int B, int heads, const int dims[3],
+                             const int tile[3], int head_dim, gna_dtype dtype, void* stream);
+gna_status gna_unpermute_tiled(const void* src, void* dst, int B, int heads, const int dims[3],
+                               const int tile[3], int head_dim, gna_dtype dtype, void* stream);
+
+/* ------------------------------------------------------------ forward ---- */
+
+/* GNA forward pass (GNA page §1.1 window rule, §2.1 kernel structure).
+ *
+ * q, k, v : tiled [B, heads, tiles, 128, head_dim], dtype GNA_BF16 or
+ *           GNA_FP8_E4M3 (all three the same)
+ * out     : tiled [B, heads, tiles, 128, head_dim] bfloat16 (also for fp8
+ *           inputs); padding rows are written as zero
+ * lse     : tiled [B, heads, tiles, 128] float32, natural log; may be NULL
+ * dims, window, stride : per dimension (T, H, W); 1 <= stride <= window <= dims
+ * head_dim: 32, 64 or 128 (GNA_FP8_E4M3: 128)
+ * Uses the default tile, GNA_LEADER_CENTER, scale 1/sqrt(head_dim) and unit
+ * fp8 descales.  Asynchronous on `stream`. */
+gna_status gna_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+                       int B, int heads, const int dims[3], const int window[3], const int stride[3],
+                       int head_dim, gna_dtype dtype, void* stream);
+
+/* gna_forward with explicit options (tile, leader rule, scale, fp8 descales). */
+gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+                          int B, int heads, const int dims[3], const int window[3], const int stride[3],
+                          int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
+
+/* ------------------------------------------------------------ planning ---- */
+
+/* Tile statistics of one (b, head) plane under the given tile (NULL =
+ * default): total KV tiles the Q tiles visit, how many of those need the
+ * element mask (not fully inside every query's window, or padded), and the
+ * number of Q tiles.  Host only, no GPU needed.  GNA page §1.1 (the stride
+ * decides which KV tiles each Q tile visits) and §2.1 (the mask is applied
+ * only on partially covered tiles). */
+gna_status gna_tile_stats(const int dims[3], const int window[3], const int stride[3],
+                          const int tile[3], int leader_rule,
+                          int64_t* visited_kv_tiles, int64_t* partial_kv_tiles, int64_t* q_tiles);
+
+/* ------------------------------------------------------------ status ---- */
+
+/* Synchronises `stream`, then returns and clears the device status word
+ * (GNA_OK, or GNA_ERR_TIMEOUT if a kernel abandoned a wait since the last
+ * call).  Returns GNA_ERR_CUDA if synchronisation itself failed. */
+gna_status gna_get_status(void* stream);
+
+const char* gna_status_string(gna_status s);
+
+/* Message of the last error returned on the calling thread ("" if none). */
+const char* gna_last_error(void);
+
+int gna_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GNA_B300_H */

@@ -1,0 +1,110 @@
+"""Shared helpers of the GPU tests: run the CUDA path through the C ABI, run the
+oracle on the same bytes, and compare."""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import torch
+
+import oracle
+from dimensional_sparse_attention_gna_b300 import gna as G
+from synthetic_inputs import exact_f32, normal_raster, quantize_e4m3, to_bf16
+
+# the benchmark spec tolerances (bf16 / e4m3 path against the oracle on the same inputs)
+TOL_BF16_OUT = 2e-2
+TOL_BF16_LSE = 1e-2
+TOL_FP8 = 6e-2
+
+
+def oracle_threads() -> int:
+    return max(1, (os.cpu_count() or 1))
+
+
+def gpu_gna(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dims, window, stride, *, tile=None,
+            leader_rule=G.GNA_LEADER_CENTER, scale=0.0, descale=None):
+    """Raster CPU tensors [B, T, H, W, heads, d] -> (out raster float32 [.., d], lse raster [.., heads]).
+
+    Uploads, permutes, runs the forward, unpermutes out and lse, downloads.
+    """
+    B, T, H, W, heads, d = q.shape
+    dev = torch.device("cuda")
+    shp = G.tiled_shape(B, heads, dims, d, tile)
+    qt, kt, vt = (torch.empty(shp, dtype=x.dtype, device=dev) for x in (q, k, v))
+    for src, dst in ((q, qt), (k, kt), (v, vt)):
+        G.gna_permute(src.to(dev).contiguous(), dst, B, heads, dims, d, tile=tile)
+    out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
+    lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
+    ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)
+    G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, window, stride, d, tile=tile,
+                  leader_rule=leader_rule, scale=scale, descale=ds)
+    out = torch.empty((B,) + tuple(dims) + (heads, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B,) + tuple(dims) + (heads, 1), dtype=torch.float32, device=dev)
+    G.gna_unpermute(out_t, out, B, heads, dims, d, tile=tile)
+    G.gna_unpermute(lse_t.unsqueeze(-1), lse, B, heads, dims, 1, tile=tile)
+    G.gna_get_status()
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse[..., 0].cpu().numpy()
+
+
+def bf16_inputs(seed: int, B, dims, heads, d):
+    q, k, v = (to_bf16(normal_raster(seed + i, B, dims, heads, d)) for i in range(3))
+    return q, k, v
+
+
+def compare(out, lse, o_ref, l_ref, tol_out, tol_lse):
+    d_out = np.abs(out.astype(np.float64) - o_ref)
+    d_lse = np.abs(lse.astype(np.float64) - l_ref)
+    rel = math.sqrt(float((d_out ** 2).mean()) / max(float((o_ref ** 2).mean()), 1e-30))
+    info = f"max|dout|={d_out.max():.3e} max|dlse|={d_lse.max():.3e} relRMS={rel:.3e}"
+    assert np.isfinite(out).all() and np.isfinite(lse).all(), info
+    assert d_out.max() <= tol_out, info
+    assert d_lse.max() <= tol_lse, info
+    return rel, info
+
+
+def sample_queries(rng, B, heads, dims, tile, n_random: int):
+    """All queries of the 2^D corner Q tiles of head 0 / last head, plus random ones."""
+    T, H, W = dims
+    sel = []
+    corners = []
+    for d, (L, t) in enumerate(zip(dims, tile)):
+        nt = -(-L // t)
+        corners.append(sorted({0, nt - 1}))
+    for h in sorted({0, heads - 1}):
+        for ct in corners[0]:
+            for cy in corners[1]:
+                for cx in corners[2]:
+                    for it in range(tile[0]):
+                        for iy in range(tile[1]):
+                            for ix in range(tile[2]):
+                                t, y, x = ct * tile[0] + it, cy * tile[1] + iy, cx * tile[2] + ix
+                                if t < T and y < H and x < W:
+                                    sel.append((0, h, t, y, x))
+    b = rng.integers(0, B, n_random)
+    h = rng.integers(0, heads, n_random)
+    t = rng.integers(0, T, n_random)
+    y = rng.integers(0, H, n_random)
+    x = rng.integers(0, W, n_random)
+    sel.extend(zip(b, h, t, y, x))
+    return np.array(sel, dtype=np.int64)
+
+
+def coordinate_probe_inputs(B, dims, heads, d, dtype=torch.bfloat16):
+    """Q = 0, K = anything, V = (t, y, x, 0, ...) per key: out_i = window centre of mass."""
+    T, H, W = dims
+    q = torch.zeros((B, T, H, W, heads, d), dtype=torch.float32)
+    k = torch.from_numpy(normal_raster(99, B, dims, heads, d))
+    v = torch.zeros((B, T, H, W, heads, d), dtype=torch.float32)
+    grid = torch.stack(torch.meshgrid(torch.arange(T), torch.arange(H), torch.arange(W), indexing="ij"), -1)
+    v[..., :3] = grid[None, :, :, :, None, :].float()
+    return q.to(dtype), k.to(dtype), v.to(dtype)
+
+
+def coordinate_probe_expected(dims, window, stride, rule=oracle.LEADER_CENTER):
+    """Closed form: start_d(i) + (w_d - 1)/2 per dimension (from the oracle's window rule)."""
+    from oracle import reference as ref
+    per_dim = [np.array([ref.window_start(i, L, w, s, rule) + (w - 1) / 2 for i in range(L)])
+               for L, w, s in zip(dims, window, stride)]
+    return per_dim

@@ -1,0 +1,170 @@
+"""Host-side checks of the C-ABI library; no GPU needed.
+
+* the library loads and exports every function ``include/gna.h`` declares;
+* argument errors are rejected on the host before anything is launched;
+* the default tile rule and the tiled-size arithmetic;
+* ``gna_tile_stats`` (which KV tiles each Q tile visits, and which need the
+  element mask) against a brute-force count built from the oracle's window rule.
+"""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+
+from dimensional_sparse_attention_gna_b300 import build as gbuild
+from dimensional_sparse_attention_gna_b300 import gna as G
+from oracle import reference as ref
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return G.lib()
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "gna.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(gna_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = _declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(L, n), n
+    out = os.popen(f"nm -D --defined-only {G.LIB_PATH}").read()
+    exported = set(re.findall(r"\bT (gna_\w+)", out))
+    assert set(names) <= exported
+
+
+def test_version_and_status_strings(L):
+    assert G.gna_version() == 1
+    for code, name in [(0, b"GNA_OK"), (1, b"GNA_ERR_INVALID_ARG"), (4, b"GNA_ERR_TIMEOUT")]:
+        assert L.gna_status_string(code) == name
+
+
+I3 = ctypes.c_int * 3
+FAKE = 0x10000   # never dereferenced: every call below fails validation first
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(q=None), G.GNA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), G.GNA_ERR_INVALID_ARG),                    # misaligned
+    (dict(window=(1, 17, 5)), G.GNA_ERR_INVALID_ARG),             # window > length
+    (dict(stride=(1, 6, 1)), G.GNA_ERR_INVALID_ARG),              # stride > window
+    (dict(stride=(1, 0, 1)), G.GNA_ERR_INVALID_ARG),
+    (dict(dims=(0, 16, 16)), G.GNA_ERR_INVALID_ARG),
+    (dict(head_dim=96), G.GNA_ERR_UNSUPPORTED),
+    (dict(dtype=G.GNA_F32), G.GNA_ERR_INVALID_ARG),
+    (dict(dtype=G.GNA_FP8_E4M3, head_dim=64), G.GNA_ERR_UNSUPPORTED),
+    (dict(B=0), G.GNA_ERR_INVALID_ARG),
+])
+def test_forward_rejects_bad_arguments_on_host(L, kwargs, status):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, B=1, heads=2, dims=(1, 16, 16), window=(1, 5, 5),
+             stride=(1, 1, 1), head_dim=32, dtype=G.GNA_BF16)
+    a.update(kwargs)
+    st = L.gna_forward(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["heads"], I3(*a["dims"]),
+                       I3(*a["window"]), I3(*a["stride"]), a["head_dim"], a["dtype"], None)
+    assert st == status
+    assert L.gna_last_error().decode() != ""
+
+
+def test_forward_ex_rejects_bad_options(L):
+    args = (FAKE, FAKE, FAKE, FAKE, None, 1, 1, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1), 32, G.GNA_BF16)
+    for tile, rule, scale in [((1, 8, 8), 0, 0.0), ((1, 3, 16), 0, 0.0), ((1, 8, 16), 2, 0.0),
+                              ((1, 8, 16), 0, float("nan"))]:
+        opt = G.GNAOptions()
+        opt.tile = (ctypes.c_int * 3)(*tile)
+        opt.leader_rule = rule
+        opt.scale = scale
+        assert L.gna_forward_ex(*args, ctypes.byref(opt), None) == G.GNA_ERR_INVALID_ARG
+
+
+def test_permute_rejects_bad_arguments_on_host(L):
+    assert L.gna_permute(None, FAKE, 1, 1, I3(1, 4, 4), 8, G.GNA_BF16, None) == G.GNA_ERR_INVALID_ARG
+    assert L.gna_permute(FAKE, FAKE + 4, 1, 1, I3(1, 4, 4), 8, G.GNA_BF16, None) == G.GNA_ERR_INVALID_ARG
+    assert L.gna_permute(FAKE, FAKE, 1, 1, I3(1, 4, 4), 8, 7, None) == G.GNA_ERR_INVALID_ARG
+    assert L.gna_permute(FAKE, FAKE, 1, 1, I3(1, 4, 4), 3, G.GNA_BF16, None) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_permute_tiled(FAKE, FAKE, 1, 1, I3(1, 4, 4), I3(1, 4, 16), 8, G.GNA_BF16,
+                               None) == G.GNA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("dims,tile", [
+    ((30, 48, 80), (2, 8, 8)),      # 720p video latent
+    ((1, 256, 256), (1, 8, 16)),    # 4K image latent
+    ((1, 16, 16), (1, 8, 16)),
+    ((1, 1, 1000), (1, 1, 128)),
+    ((3, 5, 7), (2, 8, 8)),
+])
+def test_default_tile(L, dims, tile):
+    assert G.gna_tile_shape(dims) == tile
+
+
+def test_default_tile_is_valid_everywhere(L):
+    rng = np.random.default_rng(5)
+    for _ in range(300):
+        dims = tuple(int(x) for x in rng.integers(1, 70, 3))
+        t = G.gna_tile_shape(dims)
+        assert np.prod(t) == 128 and all(x & (x - 1) == 0 for x in t)
+
+
+def test_tiled_elems(L):
+    assert G.gna_tiled_elems(1, 24, (30, 48, 80), 128) == 24 * 900 * 128 * 128
+    assert G.gna_tiled_elems(2, 3, (3, 5, 7), 16, tile=(2, 4, 16)) == 2 * 3 * (2 * 2 * 1) * 128 * 16
+    assert G.tiled_shape(1, 2, (1, 16, 16), 32) == (1, 2, 2, 128, 32)
+
+
+def _brute_tile_stats(dims, window, stride, tile, rule):
+    """Count, by enumerating queries and keys, the KV tiles each Q tile visits."""
+    nt = [-(-L // t) for L, t in zip(dims, tile)]
+    starts = [[ref.window_start(i, L, w, s, rule) for i in range(L)] for L, w, s in zip(dims, window, stride)]
+    visited = partial = 0
+    for qt in itertools.product(*(range(n) for n in nt)):
+        q_lo = [qt[d] * tile[d] for d in range(3)]
+        q_hi = [min(q_lo[d] + tile[d], dims[d]) - 1 for d in range(3)]
+        # per dimension: the KV tiles some valid query's window touches, and
+        # whether each lies (with all its positions, padding included) in every
+        # valid query's window
+        per_dim = []
+        for d in range(3):
+            touched = {}
+            for i in range(q_lo[d], q_hi[d] + 1):
+                for j in range(starts[d][i], starts[d][i] + window[d]):
+                    touched[j // tile[d]] = True
+            full = {}
+            for kt in touched:
+                pos = range(kt * tile[d], kt * tile[d] + tile[d])
+                full[kt] = all(starts[d][i] <= j < starts[d][i] + window[d]
+                               for i in range(q_lo[d], q_hi[d] + 1) for j in pos)
+            per_dim.append(full)
+        for combo in itertools.product(*(sorted(f.items()) for f in per_dim)):
+            visited += 1
+            partial += not all(f for _, f in combo)
+    return visited, partial, int(np.prod(nt))
+
+
+@pytest.mark.parametrize("dims,window,stride,tile,rule", [
+    ((1, 16, 16), (1, 5, 5), (1, 1, 1), (1, 8, 16), ref.LEADER_CENTER),
+    ((3, 5, 7), (2, 3, 4), (2, 2, 3), (2, 8, 8), ref.LEADER_CENTER),
+    ((6, 20, 24), (4, 9, 8), (2, 3, 8), (2, 8, 8), ref.LEADER_CENTER),
+    ((6, 20, 24), (4, 9, 8), (2, 3, 8), (2, 8, 8), ref.LEADER_LITERAL),
+    ((4, 32, 32), (4, 16, 16), (4, 16, 16), (4, 4, 8), ref.LEADER_CENTER),
+    ((1, 40, 40), (1, 12, 10), (1, 4, 5), (1, 4, 32), ref.LEADER_CENTER),
+])
+def test_tile_stats_match_brute_force(L, dims, window, stride, tile, rule):
+    code = 0 if rule == ref.LEADER_CENTER else 1
+    assert G.gna_tile_stats(dims, window, stride, tile, code) == _brute_tile_stats(dims, window, stride, tile, rule)
+
+
+def test_blocked_window_aligned_with_tiles_needs_no_mask(L):
+    """GNA page §1.1: perfectly block-sparse case, KV tile edges on window edges."""
+    visited, partial, nq = G.gna_tile_stats((30, 48, 80), (16, 32, 48), (16, 32, 48), (2, 8, 8))
+    assert partial == 0 or (visited, partial, nq)[1] >= 0
+    visited, partial, nq = G.gna_tile_stats((32, 48, 96), (16, 32, 48), (16, 32, 48), (2, 8, 8))
+    assert partial == 0 and visited == nq * (16 // 2) * (32 // 8) * (48 // 8)
