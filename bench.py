@@ -1,0 +1,485 @@
+"""Benchmark of the GNA forward hot path on B300.
+
+One step = one pass of the whole path over one batch of synthetic input:
+    permute Q, K, V (raster -> 128-token tiles)  ->  fused GNA forward
+    ->  unpermute O and lse (tiles -> raster)
+on the 720p-video latent workload (30 x 48 x 80 tokens, 24 heads, head_dim 128,
+window 16 x 32 x 48, bf16), the configuration the GNA page's video results and
+its Blackwell kernel throughput are about.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on
+bounded samples of the same workload instead.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--stride 1,1,1] [--heads 24]
+    torchrun --nproc-per-node N bench.py --gpus N ...
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "GNA fwd useful TFLOP/s on 1 B300 and % of dense tensor peak; speedup vs dense attn"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gna_fwd_traffic.json")
+FWD_SOURCE = os.path.join(ROOT, "dimensional_sparse_attention_gna_b300", "csrc", "gna_fwd.cu")
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--dims", default="30,48,80")
+    ap.add_argument("--window", default="16,32,48")
+    ap.add_argument("--stride", default="1,1,1")
+    ap.add_argument("--heads", type=int, default=24)
+    ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--head-dim", type=int, default=128)
+    ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    a = ap.parse_args(argv)
+    a.dims = tuple(int(x) for x in a.dims.split(","))
+    a.window = tuple(int(x) for x in a.window.split(","))
+    a.stride = tuple(int(x) for x in a.stride.split(","))
+    return a
+
+
+def useful_flops(B, heads, dims, window, d) -> float:
+    """GNA page §1.2: every query processes prod(window) keys: 2 flops per MAC, QK^T and PV."""
+    return 4.0 * B * heads * math.prod(dims) * math.prod(window) * d
+
+
+def workload_name(a) -> str:
+    kind = "3-D video" if a.dims[0] > 1 else "2-D image"
+    return (f"{kind} GNA forward {'x'.join(map(str, a.dims))} tokens, {a.heads} heads, d={a.head_dim}, "
+            f"window {'x'.join(map(str, a.window))}, stride {'x'.join(map(str, a.stride))}, B={a.batch}, {a.dtype}")
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_traffic(per_unit_heads: int, heads: int, B: int):
+    """DRAM bytes per forward launch from the committed ncu capture, scaled to this
+    launch by (b, head) planes, or None if the kernel source changed since."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)
+        with open(FWD_SOURCE, "rb") as f:
+            h = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    if rec.get("source_sha256") != h:
+        return None
+    return rec["bytes_per_plane"] * heads * B
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_setup(a):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of ``x`` over all ranks (the job's wall time is its slowest rank)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), float(parts[3]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 200.0] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "samples": len(rows), "reasons": reasons}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+
+def oracle_rate(a, seconds: float, cores: int, seed_offset: int = 0):
+    """Time the C oracle on a bounded random sample of the workload's queries.
+
+    Returns (useful flops processed, seconds, n_queries)."""
+    import oracle
+    from synthetic_inputs import exact_f32, qkv_normal, quantize_e4m3, to_bf16, normal_raster
+
+    dims, heads, d, B = a.dims, a.heads, a.head_dim, a.batch
+    # One head's worth of keys is all a sampled query touches; generate a
+    # 1-head raster of the same geometry (same per-query work) to bound memory.
+    q, k, v = qkv_normal(2 + seed_offset, B, dims, 1, d)
+    if a.dtype == "bf16":
+        qf, kf, vf = (exact_f32(to_bf16(x)) for x in (q, k, v))
+        scales = (1.0, 1.0, 1.0)
+    else:
+        qs = [quantize_e4m3(x) for x in (q, k, v)]
+        qf, kf, vf = (exact_f32(c) for c, _ in qs)
+        scales = tuple(s for _, s in qs)
+    per_query = 4.0 * math.prod(a.window) * d
+    rng = np.random.default_rng(7 + seed_offset)
+    n_all = B * math.prod(dims)
+
+    def run(n):
+        sel = rng.integers(0, n_all, n).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.forward_c(qf, kf, vf, dims, a.window, a.stride, tensor_scales=scales, sel=sel, threads=cores)
+        return time.perf_counter() - t0
+
+    n = max(cores, 8)
+    dt = run(n)
+    while dt < 0.5:
+        n *= 4
+        dt = run(n)
+    n_final = max(1, int(n * seconds / dt))
+    dt = run(n_final)
+    return per_query * n_final, dt, n_final
+
+
+def reference_arm(a, rank, world):
+    if rank != 0:
+        return
+    cores = os.cpu_count() or 1
+    per_step = max(1.0, 60.0 / max(1, a.steps + a.warmup))     # keep the whole run near a minute
+    for _ in range(a.warmup):
+        oracle_rate(a, per_step, cores)
+    flops = secs = 0.0
+    nq = 0
+    for i in range(a.steps):
+        f, s, n = oracle_rate(a, per_step, cores, seed_offset=i)
+        flops += f
+        secs += s
+        nq += n
+    value = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000.0 * secs / a.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: iid N(0,1) Q/K/V, rounded to the GPU input type",
+        "config": {"workload": workload_name(a), "dims": list(a.dims), "window": list(a.window),
+                   "stride": list(a.stride), "heads": a.heads, "B": a.batch, "head_dim": a.head_dim},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{nq} random queries of the workload over {a.steps} steps "
+                                   "(plain C oracle, float64, one thread per core)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def gpu_arm(a, rank, world, local):
+    from dimensional_sparse_attention_gna_b300 import gna as G
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    B, heads, dims, d = a.batch, a.heads, a.dims, a.head_dim
+    dt = torch.bfloat16 if a.dtype == "bf16" else torch.float8_e4m3fn
+    stream = torch.cuda.current_stream()
+
+    # inputs: iid N(0,1) drawn on the device (identical recipe to the tests'
+    # host generator in distribution; the bench times the path, not the draw)
+    gen = torch.Generator(device=dev).manual_seed(20261204 + rank)
+    raster_shape = (B,) + dims + (heads, d)
+    descale = None
+    xs = []
+    for _ in range(3):
+        x = torch.randn(raster_shape, device=dev, generator=gen, dtype=torch.float32)
+        if a.dtype == "bf16":
+            xs.append(x.to(torch.bfloat16))
+        else:
+            s = float(x.abs().max()) / 448.0
+            xs.append((x / s).to(torch.float8_e4m3fn))
+            descale = (descale or []) + [s]
+        del x
+    ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)
+    shp = G.tiled_shape(B, heads, dims, d)
+    qt, kt, vt = (torch.empty(shp, dtype=dt, device=dev) for _ in range(3))
+    out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
+    lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
+    out = torch.empty(raster_shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(raster_shape[:-1] + (1,), dtype=torch.float32, device=dev)
+
+    ev = {"fwd": [], "perm": []}
+
+    def step(record=False):
+        if record:
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+        for x, t in zip(xs, (qt, kt, vt)):
+            G.gna_permute(x, t, B, heads, dims, d, stream=stream)
+        if record:
+            e[1].record(stream)
+        G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds, stream=stream)
+        if record:
+            e[2].record(stream)
+        G.gna_unpermute(out_t, out, B, heads, dims, d, stream=stream)
+        G.gna_unpermute(lse_t.unsqueeze(-1), lse, B, heads, dims, 1, stream=stream)
+        if record:
+            e[3].record(stream)
+            ev["perm"].append((e[0], e[1]))
+            ev["fwd"].append((e[1], e[2]))
+            ev.setdefault("unperm", []).append((e[2], e[3]))
+    launches_per_step = 6
+
+    for _ in range(a.warmup):
+        step()
+    G.gna_get_status(stream)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except ValueError:
+            gpu_index = local
+    with ClockSampler(gpu_index) as clocks:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(a.steps):
+            step(record=True)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    G.gna_get_status(stream)
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    fwd_ms = statistics.mean(s.elapsed_time(e) for s, e in ev["fwd"])
+    perm_ms = statistics.mean(s.elapsed_time(e) for s, e in ev["perm"])
+    unperm_ms = statistics.mean(s.elapsed_time(e) for s, e in ev["unperm"])
+    flops_rank = useful_flops(B, heads, dims, a.window, d)
+    total_flops = sum_over_ranks(flops_rank * a.steps, world)
+    value = total_flops / (elapsed_ms / 1e3) / 1e12
+    kernel_tflops = flops_rank / (fwd_ms / 1e3) / 1e12
+    esz = torch.tensor([], dtype=dt).element_size()
+    perm_bytes = 3 * 2 * B * math.prod(dims) * heads * d * esz
+    unperm_bytes = 2 * B * math.prod(dims) * heads * (d * 2 + 4)
+
+    peaks, peaks_kind = load_peaks()
+    pk = "bf16_tflops_sustained" if a.dtype == "bf16" else "bf16_tflops_sustained"
+    peak = peaks.get(pk, FALLBACK_PEAKS["bf16_tflops_sustained"])
+    if a.dtype == "fp8":
+        peak *= 2.0     # fp8 dense rate is twice bf16 (nominal 4.5 vs 2.25 PFLOP/s)
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * (2.0 if a.dtype == "fp8" else 1.0)
+
+    # tile-level work of the launch (what the tensor cores execute)
+    visited, partial, nq = G.gna_tile_stats(dims, a.window, a.stride)
+    tile_flops = 4.0 * B * heads * visited * 128 * 128 * d
+
+    # dense attention through the same kernel on the same tokens (window = grid)
+    speedup = None
+    dense_ms = None
+    if not a.no_dense:
+        for _ in range(1):
+            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, dims, (1, 1, 1), d, descale=ds, stream=stream)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 2
+        e0.record(stream)
+        for _ in range(reps):
+            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, dims, (1, 1, 1), d, descale=ds, stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        G.gna_get_status(stream)
+        dense_ms = e0.elapsed_time(e1) / reps
+        speedup = dense_ms / fwd_ms
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not a.no_e2e:
+        host_in = [x.cpu().pin_memory() for x in xs]
+        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        dev_in = [torch.empty_like(x) for x in xs]
+
+        def e2e_step():
+            for h, dv in zip(host_in, dev_in):
+                dv.copy_(h, non_blocking=True)
+            for x, t in zip(dev_in, (qt, kt, vt)):
+                G.gna_permute(x, t, B, heads, dims, d, stream=stream)
+            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds,
+                          stream=stream)
+            G.gna_unpermute(out_t, out, B, heads, dims, d, stream=stream)
+            G.gna_unpermute(lse_t.unsqueeze(-1), lse, B, heads, dims, 1, stream=stream)
+            host_out.copy_(out, non_blocking=True)
+            host_lse.copy_(lse, non_blocking=True)
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(a.steps, 5))
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e_val = sum_over_ranks(flops_rank * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
+        e2e = {"value": e2e_val, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(sum(x.numel() * x.element_size() for x in host_in)),
+               "d2h_bytes_per_step": int(host_out.numel() * host_out.element_size()
+                                         + host_lse.numel() * host_lse.element_size())}
+
+    clk = clocks.summary()
+    traffic = kernel_traffic(1, heads, B)
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        f, s, n = oracle_rate(a, a.cpu_seconds, cores)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} random queries of the workload (one synthetic head), plain C oracle, float64, "
+                         f"{s:.1f} s on {cores} threads"}
+
+    if rank != 0:
+        return
+    n_ratio = math.prod(dims) / math.prod(a.window)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": a.dtype,
+        "data": "synthetic: iid N(0,1) Q/K/V drawn on the device per rank",
+        "config": {"workload": workload_name(a), "dims": list(dims), "window": list(a.window),
+                   "stride": list(a.stride), "heads": heads, "B": B, "head_dim": d,
+                   "tile": list(G.gna_tile_shape(dims)),
+                   "l2": "inputs larger than L2 (3 x %.0f MB raster + tiled copies)" % (
+                       B * math.prod(dims) * heads * d * esz / 1e6),
+                   "parallelism": f"replicas x{world}: every rank runs the full workload on its own data"},
+        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": kernel_tflops / peak, "traffic": traffic,
+                     "peak_source": f"{peaks_kind} {'bf16' if a.dtype == 'bf16' else 'fp8 (2x bf16)'} sustained",
+                     "frac_of_burst_peak": kernel_tflops / peak_burst,
+                     "tile_work_tflops": tile_flops / (fwd_ms / 1e3) / 1e12,
+                     "tile_overhead": tile_flops / flops_rank, "partial_tile_share": partial / visited},
+        "kernels_ms": {"permute_qkv": perm_ms, "forward": fwd_ms, "unpermute_o_lse": unperm_ms},
+        "permute_gbps": perm_bytes / (perm_ms / 1e3) / 1e9,
+        "permute_frac_of_hbm": perm_bytes / (perm_ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6400.0),
+        "unpermute_gbps": unperm_bytes / (unperm_ms / 1e3) / 1e9,
+        "dense_forward_ms": dense_ms, "speedup_vs_dense": speedup,
+        "flop_sparsity_ratio": n_ratio,
+        "speedup_over_ratio": None if speedup is None else speedup / n_ratio,
+        "e2e": e2e, "gpu_launches": launches_per_step * a.steps, "clocks": clk, "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    a = parse_args(argv)
+    rank, world, local = dist_setup(a)
+    try:
+        if a.impl == "reference":
+            reference_arm(a, rank, world)
+        else:
+            gpu_arm(a, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

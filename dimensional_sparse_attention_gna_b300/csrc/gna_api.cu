@@ -346,7 +346,7 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out
     p.fault_skip_kv = -1;
     if (const char* f = std::getenv("GNA_TEST_SKIP_KV_LOAD")) p.fault_skip_kv = std::atoi(f);
 
-    if ((st = make_tile_map(&p.tmQ, q, rows, head_dim, es)) != GNA_OK) return st;
+    p.q = q;
     if ((st = make_tile_map(&p.tmK, k, rows, head_dim, es)) != GNA_OK) return st;
     if ((st = make_tile_map(&p.tmV, v, rows, head_dim, es)) != GNA_OK) return st;
 

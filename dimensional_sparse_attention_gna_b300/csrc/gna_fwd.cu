@@ -7,27 +7,30 @@
 //        tiles with TMA.
 //  §2.1  the element mask is applied only to KV tiles that are not entirely
 //        inside the attention window; loads overlap compute.
-//  §1.2  Q-tile and KV-tile sizes are decoupled.
 // Video tutorial page ("视频生成推理提速:稀疏注意力组合配置教程"), §3.3: the
 // softmax is accumulated block by block and the n x n matrix never exists.
 //
 // One CTA owns one 128-query tile of one (batch, head) and walks the box of
-// KV tiles its windows touch.  Warp roles (192 threads):
-//   warp 0      TMA producer: Q once, then K and V through NS-stage rings
-//   warp 1      TMEM allocator and tcgen05.mma issuer (one elected lane)
-//   warps 2..5  softmax + correction + epilogue; thread = one query row,
-//               TMEM lane quarter = warp % 4
-// TMEM (512 columns): O at [0, 128), S double buffer at [128, 256) and
-// [256, 384).  P overwrites the front of its S buffer (bf16: 64 columns,
-// e4m3: 32 columns) and feeds the P*V MMA straight from TMEM.
+// KV tiles its windows touch.  Warp roles (320 threads):
+//   warp 0      TMA producer: K and V tiles through NS-stage mbarrier rings
+//   warp 1      TMEM allocator and tcgen05.mma issuer (lane 0)
+//   warps 2..9  softmax / correction / epilogue.  Thread = (query row, half):
+//               warps 2..5 own score columns [0, 64) of their 32 rows, warps
+//               6..9 columns [64, 128) (TMEM lane quarter = warp % 4).  The two
+//               halves of a row swap their partial maxima through shared
+//               memory once per tile; row sums stay partial until the end.
+// TMEM (512 columns): O [0, 128), S double buffer [128, 256) and [256, 384),
+// Q [384, 384 + head_dim * elem / 4).  Q sits in TMEM so S = Q K^T reads only
+// K from shared memory; P overwrites the front of its S buffer (bf16: 64
+// columns, e4m3: 32) and feeds O += P V straight from TMEM.
 // MMA issue order  QK(0) QK(1) PV(0) QK(2) PV(1) ...  keeps the tensor core on
 // the next S while the softmax warps work on the current one.
 //
-// The running row maximum is updated lazily: the output accumulator is only
-// rescaled when the maximum grows by more than kTau (log2 units); between
-// rescales P may exceed 1 by up to 2^kTau, which the final O / l cancels
-// exactly.  For e4m3 P the exponent is shifted by kP8Shift so that P uses the
-// normal range of e4m3 (values up to 2^(kP8Shift + kTau) <= 448).
+// The running row maximum is updated lazily: O is rescaled only when the
+// maximum grows by more than `tau` (log2 units); in between P may exceed 1 by
+// up to 2^tau, which the final O / l cancels exactly.  For e4m3 P the exponent
+// is shifted by `p_shift` so that P uses the normal range of e4m3 (at most
+// 2^(p_shift + tau) <= 448).
 //
 // Every mbarrier wait is bounded (see ptx.cuh); a role that gives up raises
 // the CTA abort flag and the device status word, the other roles drop out of
@@ -48,11 +51,12 @@ __device__ int g_device_status = 0;
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kSoftmaxWarp0 = 2;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxWarps = 8;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS0 = 128;
+constexpr uint32_t kColQ = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -73,24 +77,26 @@ struct Precision<1> {                       // e4m3 inputs, e4m3 P
 
 template <int D, int ESZ, int NS>
 struct Cfg {
-    static constexpr int kRowBytes = (D * ESZ) >= 128 ? 128 : D * ESZ;      // swizzle span
-    static constexpr int kChunks = (D * ESZ) / kRowBytes;                    // TMA boxes per tile
+    static constexpr int kRowBytesAll = D * ESZ;                             // bytes of one token row
+    static constexpr int kRowBytes = kRowBytesAll >= 128 ? 128 : kRowBytesAll;   // swizzle span
+    static constexpr int kChunks = kRowBytesAll / kRowBytes;                 // TMA boxes per tile
     static constexpr int kChunkElems = kRowBytes / ESZ;
     static constexpr uint32_t kSwizzle = kRowBytes == 128 ? kSwizzle128B : kRowBytes == 64 ? kSwizzle64B : kSwizzle32B;
-    static constexpr int kTileBytes = kTileElems * D * ESZ;
-    static constexpr int kSmemQ = 0;
-    static constexpr int kSmemK = kTileBytes;
-    static constexpr int kSmemV = kTileBytes * (1 + NS);
-    static constexpr int kSmemData = kTileBytes * (1 + 2 * NS);
+    static constexpr int kTileBytes = kTileElems * kRowBytesAll;
+    static constexpr int kSmemK = 0;
+    static constexpr int kSmemV = kTileBytes * NS;
+    static constexpr int kSmemData = kTileBytes * 2 * NS;
     // at least ~116 KB so that only one CTA (which owns all 512 TMEM columns)
     // is resident per SM
     static constexpr int kSmemAlloc = (kSmemData + 1024) > 118784 ? (kSmemData + 1024) : 118784;
     static constexpr int kKPerInstr = 32 / ESZ;                              // MMA K extent (elements)
-    static constexpr int kQKSteps = D / kKPerInstr;
+    static constexpr int kQKSteps = kRowBytesAll / 32;
     static constexpr int kPVSteps = kTileElems / kKPerInstr;
     static constexpr uint32_t kIdescQK = make_idesc(128, 128, Precision<ESZ>::fmt, false);
     static constexpr uint32_t kIdescPV = make_idesc(128, D, Precision<ESZ>::fmt, true);
-    static constexpr int kPCols = kTileElems * ESZ / 4;                      // TMEM columns of P
+    static constexpr int kQHalfWords = kRowBytesAll / 8;                     // TMEM columns of half a Q row
+    static constexpr int kPHalfWords = 64 * ESZ / 4;                         // TMEM columns of half a P row
+    static constexpr int kOHalf = D / 2;                                     // O columns per half
 };
 
 struct Barriers {
@@ -106,6 +112,37 @@ __device__ __forceinline__ float fast_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// (a.x * b.x + c.x, a.y * b.y + c.y) in one packed instruction
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    uint64_t ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    uint64_t ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
 }
 
 __device__ __forceinline__ void raise_status(volatile int* abort_flag)
@@ -126,6 +163,15 @@ struct KvBox {
     }
 };
 
+__device__ __forceinline__ void advance_odometer(int (&kc)[3], const KvBox& box)
+{
+    if (++kc[2] < box.k0[2] + box.cnt[2]) return;
+    kc[2] = box.k0[2];
+    if (++kc[1] < box.k0[1] + box.cnt[1]) return;
+    kc[1] = box.k0[1];
+    ++kc[0];
+}
+
 __device__ __forceinline__ uint32_t range_bits32(int lo, int hi)
 {
     // bits [lo, hi) clipped to [0, 32)
@@ -136,70 +182,116 @@ __device__ __forceinline__ uint32_t range_bits32(int lo, int hi)
     return width_mask << lo;
 }
 
-// 128-bit column mask of one query row against KV tile kc: bit c set iff the
-// key at tile element c lies in the row's window in every dimension.
-__device__ __forceinline__ void build_row_mask(const FwdParams& p, const int (&kc)[3], const int (&st)[3],
-                                               uint32_t (&m)[4])
+// Word `wi` (tile elements 32*wi .. 32*wi+31) of the column mask of one query
+// row against one KV tile: bit set iff that key lies in the row's window in
+// every dimension.  lo_* = the row's window start relative to the tile origin.
+__device__ __forceinline__ uint32_t row_mask_word(const FwdParams& p, int wi, int lo_t, int lo_y, int lo_x)
 {
-    const int lo_t = st[0] - kc[0] * p.tile[0];
-    const int lo_y = st[1] - kc[1] * p.tile[1];
-    const int lo_x = st[2] - kc[2] * p.tile[2];
     const int tw = p.tile[2];
     const int lw = p.tlog[2];
     const int lh = p.tlog[1];
-#pragma unroll
-    for (int wi = 0; wi < 4; ++wi) {
-        uint32_t bits = 0;
-        if (tw >= 32) {
-            const int c0 = wi * 32;
-            const int g = c0 >> lw;
-            const int cy = g & ((1 << lh) - 1);
-            const int ct = g >> lh;
-            const int bx = c0 & (tw - 1);
-            const bool ok = static_cast<unsigned>(ct - lo_t) < static_cast<unsigned>(p.win[0]) &&
-                            static_cast<unsigned>(cy - lo_y) < static_cast<unsigned>(p.win[1]);
-            bits = ok ? range_bits32(lo_x - bx, lo_x - bx + p.win[2]) : 0u;
-        } else {
-            const uint32_t mx = range_bits32(lo_x, lo_x + p.win[2]) & ((1u << tw) - 1u);
-            const int groups = 32 >> lw;
-            for (int gi = 0; gi < groups; ++gi) {
-                const int g = (wi * 32 >> lw) + gi;
-                const int cy = g & ((1 << lh) - 1);
-                const int ct = g >> lh;
-                const bool ok = static_cast<unsigned>(ct - lo_t) < static_cast<unsigned>(p.win[0]) &&
-                                static_cast<unsigned>(cy - lo_y) < static_cast<unsigned>(p.win[1]);
-                if (ok) bits |= mx << (gi * tw);
-            }
-        }
-        m[wi] = bits;
+    if (tw >= 32) {
+        const int c0 = wi * 32;
+        const int g = c0 >> lw;
+        const int cy = g & ((1 << lh) - 1);
+        const int ct = g >> lh;
+        const int bx = c0 & (tw - 1);
+        const bool ok = static_cast<unsigned>(ct - lo_t) < static_cast<unsigned>(p.win[0]) &&
+                        static_cast<unsigned>(cy - lo_y) < static_cast<unsigned>(p.win[1]);
+        return ok ? range_bits32(lo_x - bx, lo_x - bx + p.win[2]) : 0u;
     }
+    const uint32_t mx = range_bits32(lo_x, lo_x + p.win[2]) & ((1u << tw) - 1u);
+    const int groups = 32 >> lw;
+    uint32_t bits = 0;
+    for (int gi = 0; gi < groups; ++gi) {
+        const int g = ((wi * 32) >> lw) + gi;
+        const int cy = g & ((1 << lh) - 1);
+        const int ct = g >> lh;
+        const bool ok = static_cast<unsigned>(ct - lo_t) < static_cast<unsigned>(p.win[0]) &&
+                        static_cast<unsigned>(cy - lo_y) < static_cast<unsigned>(p.win[1]);
+        if (ok) bits |= mx << (gi * tw);
+    }
+    return bits;
 }
 
 template <int ESZ>
-__device__ __forceinline__ void pack_p(const float (&x)[32], uint32_t* out);
+__device__ __forceinline__ void pack_p(const float (&x)[64], uint32_t (&out)[64 * ESZ / 4]);
 
 template <>
-__device__ __forceinline__ void pack_p<2>(const float (&x)[32], uint32_t* out)
+__device__ __forceinline__ void pack_p<2>(const float (&x)[64], uint32_t (&out)[32])
 {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 32; ++i) {
         __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
         out[i] = *reinterpret_cast<uint32_t*>(&h);
     }
 }
 
 template <>
-__device__ __forceinline__ void pack_p<1>(const float (&x)[32], uint32_t* out)
+__device__ __forceinline__ void pack_p<1>(const float (&x)[64], uint32_t (&out)[16])
 {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
         const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i], x[4 * i + 1]), __NV_SATFINITE, __NV_E4M3);
         const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * i + 2], x[4 * i + 3]), __NV_SATFINITE, __NV_E4M3);
         out[i] = (lo & 0xffffu) | (hi << 16);
     }
 }
 
-template <int D, int ESZ, int NS>
+// Orders later uses of registers filled by tcgen05.ld after the preceding
+// tcgen05.wait::ld (the compiler sees the registers redefined here).
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[N])
+{
+#pragma unroll
+    for (int i = 0; i < N; i += 8)
+        asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]),
+                     "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+// Store N (8, 16 or 32) consecutive 32-bit TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_store_n(uint32_t taddr, const uint32_t* r)
+{
+    if constexpr (N == 32) {
+        uint32_t a[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) a[i] = r[i];
+        tmem_st32(taddr, a);
+    } else if constexpr (N == 16) {
+        uint32_t a[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) a[i] = r[i];
+        tmem_st16(taddr, a);
+    } else {
+        static_assert(N == 8, "8, 16 or 32 columns");
+        uint32_t a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = r[i];
+        tmem_st8(taddr, a);
+    }
+}
+
+// Multiply O columns [0, N) at taddr of this thread's row by alpha (N multiple of 16).
+template <int N>
+__device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha)
+{
+#pragma unroll
+    for (int c = 0; c < N; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(taddr + c, r);
+        tmem_wait_ld();
+        reg_fence(r);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+        tmem_st16(taddr + c, r);
+    }
+    tmem_wait_st();
+}
+
+// TT, TH, TW: the layout tile when known at compile time (the default tiles),
+// or 0, 0, 0 for any tile (runtime shape, slower mask construction).
+template <int D, int ESZ, int NS, int TT, int TH, int TW>
 __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_constant__ FwdParams p)
 {
     using C = Cfg<D, ESZ, NS>;
@@ -208,6 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     __shared__ Barriers bars;
     __shared__ uint32_t tmem_base_sh;
     __shared__ volatile int abort_flag;
+    __shared__ float xchg[2][2][kTileElems];        // [tile parity][half][row]: partial row maxima / sums
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -230,14 +323,13 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     const int n_kv = box.cnt[0] * box.cnt[1] * box.cnt[2];
     const int64_t kv_row_base = bh * p.tiles_per_head * kTileElems;
 
-    const uint32_t sQ = smem_u32(smem + C::kSmemQ);
     const uint32_t sK = smem_u32(smem + C::kSmemK);
     const uint32_t sV = smem_u32(smem + C::kSmemV);
     auto bar = [](uint64_t& b) { return smem_u32(&b); };
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(bar(bars.q_full), 1);
+        mbar_init(bar(bars.q_full), kSoftmaxWarps);
         for (int s = 0; s < NS; ++s) {
             mbar_init(bar(bars.k_full[s]), 1);
             mbar_init(bar(bars.k_empty[s]), 1);
@@ -246,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(bars.s_full[s]), 1);
-            mbar_init(bar(bars.p_full[s]), 4);
+            mbar_init(bar(bars.p_full[s]), kSoftmaxWarps);
         }
         mbar_init(bar(bars.o_done), 1);
         mbar_init(bar(bars.drain), 1);
@@ -261,106 +353,154 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     tc_fence_after();
     const uint32_t tmem = tmem_base_sh;
 
+    // The producer and MMA warps run converged: every lane polls the
+    // barriers, one elected lane issues the TMA copies / MMAs / commits, so
+    // the addresses and descriptors stay warp-uniform.
     if (warp == 0) {
         // ============================================================ TMA producer
-        if (lane == 0) {
-            prefetch_tensormap(&p.tmQ);
+        if (elect_one_sync()) {
             prefetch_tensormap(&p.tmK);
             prefetch_tensormap(&p.tmV);
-            const int32_t q_row = static_cast<int32_t>(q_tile_global * kTileElems);
-            mbar_arrive_expect_tx(bar(bars.q_full), C::kTileBytes);
-            for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(sQ + c * kTileElems * C::kRowBytes, &p.tmQ, bar(bars.q_full), c * C::kChunkElems, q_row);
-            int k_issued = 0, v_issued = 0;          // KV tiles whose K / V loads were issued
-            bool early = false;
-            for (int j = 0; j < n_kv; ++j) {
-                const int s = j % NS;
-                const uint32_t ph = ((j / NS) & 1) ^ 1;
-                int kc[3];
-                box.coords(j, kc);
-                const int tile_id = (kc[0] * p.nt[1] + kc[1]) * p.nt[2] + kc[2];
-                const int32_t row = static_cast<int32_t>(kv_row_base + static_cast<int64_t>(tile_id) * kTileElems);
-                if (j >= NS && !mbar_wait(bar(bars.k_empty[s]), ph, &abort_flag)) { early = true; break; }
-                if (j == p.fault_skip_kv) { early = true; break; }   // test hook: consumers wait in vain
+        }
+        int k_issued = 0, v_issued = 0;              // KV tiles whose K / V loads were issued
+        bool early = false;
+        int kc[3] = {box.k0[0], box.k0[1], box.k0[2]};
+        for (int j = 0; j < n_kv; ++j, advance_odometer(kc, box)) {
+            const int s = j % NS;
+            const uint32_t ph = ((j / NS) & 1) ^ 1;
+            const int tile_id = (kc[0] * p.nt[1] + kc[1]) * p.nt[2] + kc[2];
+            const int32_t row = static_cast<int32_t>(kv_row_base + static_cast<int64_t>(tile_id) * kTileElems);
+            if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(bar(bars.k_empty[s]), ph, &abort_flag))) {
+                early = true;
+                break;
+            }
+            if (j == p.fault_skip_kv) { early = true; break; }   // test hook: consumers wait in vain
+            if (elect_one_sync()) {
                 mbar_arrive_expect_tx(bar(bars.k_full[s]), C::kTileBytes);
+#pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_2d(sK + s * C::kTileBytes + c * kTileElems * C::kRowBytes, &p.tmK, bar(bars.k_full[s]),
                                 c * C::kChunkElems, row);
-                ++k_issued;
-                if (j >= NS && !mbar_wait(bar(bars.v_empty[s]), ph, &abort_flag)) { early = true; break; }
+            }
+            __syncwarp();
+            ++k_issued;
+            if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(bar(bars.v_empty[s]), ph, &abort_flag))) {
+                early = true;
+                break;
+            }
+            if (elect_one_sync()) {
                 mbar_arrive_expect_tx(bar(bars.v_full[s]), C::kTileBytes);
+#pragma unroll
                 for (int c = 0; c < C::kChunks; ++c)
                     tma_load_2d(sV + s * C::kTileBytes + c * kTileElems * C::kRowBytes, &p.tmV, bar(bars.v_full[s]),
                                 c * C::kChunkElems, row);
-                ++v_issued;
             }
-            if (early) {
-                if (p.fault_skip_kv < 0) raise_status(&abort_flag);
-                // Drain: wait (bounded, ignoring the abort flag) for the loads
-                // still in flight so that no TMA write lands after the CTA exits.
-                const volatile int never = 0;
-                for (int j = (k_issued > NS ? k_issued - NS : 0); j < k_issued; ++j)
-                    mbar_wait(bar(bars.k_full[j % NS]), (j / NS) & 1, &never);
-                for (int j = (v_issued > NS ? v_issued - NS : 0); j < v_issued; ++j)
-                    mbar_wait(bar(bars.v_full[j % NS]), (j / NS) & 1, &never);
-                mbar_wait(bar(bars.q_full), 0, &never);
-            }
+            __syncwarp();
+            ++v_issued;
+        }
+        if (early) {
+            if (p.fault_skip_kv < 0 && lane == 0) raise_status(&abort_flag);
+            // Drain: wait (bounded, ignoring the abort flag) for the loads
+            // still in flight so that no TMA write lands after the CTA exits.
+            const volatile int never = 0;
+            for (int j = (k_issued > NS ? k_issued - NS : 0); j < k_issued; ++j)
+                mbar_wait(bar(bars.k_full[j % NS]), (j / NS) & 1, &never);
+            for (int j = (v_issued > NS ? v_issued - NS : 0); j < v_issued; ++j)
+                mbar_wait(bar(bars.v_full[j % NS]), (j / NS) & 1, &never);
         }
     } else if (warp == 1) {
         // ============================================================ MMA issuer
-        if (lane == 0) {
-            const uint32_t tS[2] = {tmem + kColS0, tmem + kColS0 + 128};
-            const uint32_t tO = tmem + kColO;
-            auto issue_pv = [&](int i) -> bool {
-                const int s = i % NS;
-                if (!mbar_wait(bar(bars.v_full[s]), (i / NS) & 1, &abort_flag)) return false;
-                if (!mbar_wait(bar(bars.p_full[i & 1]), (i >> 1) & 1, &abort_flag)) return false;
-                tc_fence_after();
-                const uint32_t vbase = sV + s * C::kTileBytes;
+        const uint32_t tO = tmem + kColO;
+        const uint32_t tQ = tmem + kColQ;
+        // descriptors of stage 0, chunk 0; stage / k-step offsets are added
+        // to the start-address field (addresses >> 4 stay below 2^14)
+        const uint64_t dK0 = make_smem_desc(sK, 16, 8 * C::kRowBytes, C::kSwizzle);
+        const uint64_t dV0 = make_smem_desc(sV, kTileElems * C::kRowBytes, 8 * C::kRowBytes, C::kSwizzle);
+        auto issue_pv = [&](int i) -> bool {
+            const int s = i % NS;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.v_full[s]), (i / NS) & 1, &abort_flag))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.p_full[i & 1]), (i >> 1) & 1, &abort_flag))) return false;
+            tc_fence_after();
+            if (elect_one_sync()) {
+                const uint64_t dv = dV0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
+                const uint32_t tP = tmem + kColS0 + (i & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < C::kPVSteps; ++kk) {
-                    const uint64_t dv = make_smem_desc(vbase + kk * C::kKPerInstr * C::kRowBytes,
-                                                       kTileElems * C::kRowBytes, 8 * C::kRowBytes, C::kSwizzle);
-                    if (ESZ == 2) mma_f16_ts(tO, tS[i & 1] + kk * 8, dv, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                    else mma_f8_ts(tO, tS[i & 1] + kk * 8, dv, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                    const uint64_t d = dv + static_cast<uint64_t>((kk * C::kKPerInstr * C::kRowBytes) >> 4);
+                    if (ESZ == 2) mma_f16_ts(tO, tP + kk * 8, d, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                    else mma_f8_ts(tO, tP + kk * 8, d, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(bars.o_done));
                 if (i + NS < n_kv) mma_commit(bar(bars.v_empty[s]));
-                return true;
-            };
-            bool ok = mbar_wait(bar(bars.q_full), 0, &abort_flag);
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int s = j % NS;
-                if (!mbar_wait(bar(bars.k_full[s]), (j / NS) & 1, &abort_flag)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t kbase = sK + s * C::kTileBytes;
+            }
+            __syncwarp();
+            return true;
+        };
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.q_full), 0, &abort_flag));
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const int s = j % NS;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.k_full[s]), (j / NS) & 1, &abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (elect_one_sync()) {
+                const uint64_t dk = dK0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
+                const uint32_t tS = tmem + kColS0 + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
-                    const int byte = kk * 32;
-                    const uint32_t off = (byte / C::kRowBytes) * kTileElems * C::kRowBytes + (byte % C::kRowBytes);
-                    const uint64_t da = make_smem_desc(sQ + off, 16, 8 * C::kRowBytes, C::kSwizzle);
-                    const uint64_t db = make_smem_desc(kbase + off, 16, 8 * C::kRowBytes, C::kSwizzle);
-                    if (ESZ == 2) mma_f16_ss(tS[j & 1], da, db, C::kIdescQK, kk > 0 ? 1u : 0u);
-                    else mma_f8_ss(tS[j & 1], da, db, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    constexpr int kChunkStride = kTileElems * C::kRowBytes;
+                    const int off = ((kk * 32) / C::kRowBytes) * kChunkStride + ((kk * 32) % C::kRowBytes);
+                    const uint64_t d = dk + static_cast<uint64_t>(off >> 4);
+                    if (ESZ == 2) mma_f16_ts(tS, tQ + kk * 8, d, C::kIdescQK, kk > 0 ? 1u : 0u);
+                    else mma_f8_ts(tS, tQ + kk * 8, d, C::kIdescQK, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(bars.s_full[j & 1]));
                 if (j + NS < n_kv) mma_commit(bar(bars.k_empty[s]));
-                if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
             }
-            if (ok) ok = issue_pv(n_kv - 1);
-            if (!ok) {
+            __syncwarp();
+            if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        }
+        if (ok) ok = issue_pv(n_kv - 1);
+        if (!ok) {
+            // wait for every MMA issued so far before TMEM is released
+            if (elect_one_sync()) {
                 raise_status(&abort_flag);
-                // wait for every MMA issued so far before TMEM is released
-                const volatile int never = 0;
                 mma_commit(bar(bars.drain));
-                mbar_wait(bar(bars.drain), 0, &never);
             }
+            __syncwarp();
+            const volatile int never = 0;
+            mbar_wait(bar(bars.drain), 0, &never);
         }
     } else {
         // ============================================================ softmax / correction / epilogue
         const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
         const int row = quarter * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const uint32_t pair_bar = 1 + quarter;            // named barrier of the two warps sharing these rows
+
+        // Q row -> TMEM (A operand of S = Q K^T)
+        {
+            constexpr int W = C::kQHalfWords;
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const uint8_t*>(p.q) + (q_tile_global * kTileElems + row) * C::kRowBytesAll +
+                half * (C::kRowBytesAll / 2));
+            uint32_t qw[W];
+#pragma unroll
+            for (int i = 0; i < W / 4; ++i) {
+                const uint4 v = __ldg(src + i);
+                qw[4 * i] = v.x;
+                qw[4 * i + 1] = v.y;
+                qw[4 * i + 2] = v.z;
+                qw[4 * i + 3] = v.w;
+            }
+            tmem_store_n<W>(tmem + kColQ + lane_addr + half * W, qw);
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars.q_full));
+        }
 
         // query coordinates of this row and its window starts
         int qpos[3], st[3];
@@ -386,49 +526,109 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         constexpr float kShift = Precision<ESZ>::p_shift;
 
         float m_run = -INFINITY;   // running reference maximum, log2 units (scaled scores)
-        float l_run = 0.0f;        // running sum of P (in the same shifted units as P)
+        float l_run = 0.0f;        // this half's running sum of P (same shifted units as P)
         bool ok = true;
+        const uint32_t t_ohalf = tmem + kColO + lane_addr + half * C::kOHalf;
 
-        for (int j = 0; j < n_kv; ++j) {
+        // A failed wait never leaves the loop early: the two warps sharing
+        // these rows meet at a named barrier every tile, so a warp that gives
+        // up raises the abort flag and keeps iterating without doing work
+        // until both have passed the same number of barriers.
+        int kc[3] = {box.k0[0], box.k0[1], box.k0[2]};   // KV tile of iteration j (row-major odometer)
+        for (int j = 0; j < n_kv; ++j, advance_odometer(kc, box)) {
             const int sb = j & 1;
-            ok = mbar_wait(bar(bars.s_full[sb]), (j >> 1) & 1, &abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-            tc_fence_after();
-
-            int kc[3];
-            box.coords(j, kc);
-            bool full = true;
+            if (ok) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full[sb]), (j >> 1) & 1, &abort_flag));
+                if (!ok) raise_status(&abort_flag);
+            }
+            const uint32_t t_s = tmem + kColS0 + sb * 128 + lane_addr;
+            float s[64];
+            float mx = -INFINITY;
+            if (ok) {
+                tc_fence_after();
+                uint32_t r0[32], r1[32];
+                tmem_ld32(t_s + half * 64, r0);
+                tmem_ld32(t_s + half * 64 + 32, r1);
+                // while the scores travel from TMEM: is this KV tile partial?
+                bool full = true;
 #pragma unroll
-            for (int d = 0; d < 3; ++d)
-                full = full && dim_tile_full(kc[d], p.tile[d], p.dims[d], p.win[d], box.r[d]);
-
-            float s[128];
-            {
-                uint32_t r0[32], r1[32], r2[32], r3[32];
-                const uint32_t ts = tmem + kColS0 + sb * 128 + lane_addr;
-                tmem_ld32(ts, r0);
-                tmem_ld32(ts + 32, r1);
-                tmem_ld32(ts + 64, r2);
-                tmem_ld32(ts + 96, r3);
-                tmem_wait_ld();
+                for (int d = 0; d < 3; ++d)
+                    full = full && dim_tile_full(kc[d], p.tile[d], p.dims[d], p.win[d], box.r[d]);
+                const int lo_t = st[0] - kc[0] * p.tile[0];
+                const int lo_y = st[1] - kc[1] * p.tile[1];
+                const int lo_x = st[2] - kc[2] * p.tile[2];
+                if constexpr (TW > 0) {
+                    // element (ct, cy, cx) of the tile is masked iff one of
+                    // its coordinates leaves the row's window: add -inf
+                    // biases per x position and per (t, y) group of TW columns
+                    constexpr int GPH = 64 / TW;          // (t, y) groups per half row
+                    float bx[TW], bg[GPH];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    s[i] = __uint_as_float(r0[i]);
-                    s[32 + i] = __uint_as_float(r1[i]);
-                    s[64 + i] = __uint_as_float(r2[i]);
-                    s[96 + i] = __uint_as_float(r3[i]);
+                    for (int cx = 0; cx < TW; ++cx)
+                        bx[cx] = static_cast<unsigned>(cx - lo_x) < static_cast<unsigned>(p.win[2]) ? 0.0f : -INFINITY;
+#pragma unroll
+                    for (int gi = 0; gi < GPH; ++gi) {
+                        const int g = half * GPH + gi;
+                        const int cy = g % TH, ct = g / TH;
+                        bg[gi] = (static_cast<unsigned>(ct - lo_t) < static_cast<unsigned>(p.win[0]) &&
+                                  static_cast<unsigned>(cy - lo_y) < static_cast<unsigned>(p.win[1]))
+                                     ? 0.0f : -INFINITY;
+                    }
+                    tmem_wait_ld();
+                    reg_fence(r0);
+                    reg_fence(r1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        s[i] = __uint_as_float(r0[i]);
+                        s[32 + i] = __uint_as_float(r1[i]);
+                    }
+                    if (!full) {
+#pragma unroll
+                        for (int c = 0; c < 64; c += 2) {
+                            float2 v = fadd2(make_float2(s[c], s[c + 1]), make_float2(bx[c % TW], bx[(c + 1) % TW]));
+                            v = fadd2(v, make_float2(bg[c / TW], bg[c / TW]));
+                            s[c] = v.x;
+                            s[c + 1] = v.y;
+                        }
+                    }
+                } else {
+                    uint32_t m0 = 0xffffffffu, m1 = 0xffffffffu;
+                    if (!full) {
+                        m0 = row_mask_word(p, 2 * half, lo_t, lo_y, lo_x);
+                        m1 = row_mask_word(p, 2 * half + 1, lo_t, lo_y, lo_x);
+                    }
+                    tmem_wait_ld();
+                    reg_fence(r0);
+                    reg_fence(r1);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        s[i] = __uint_as_float(r0[i]);
+                        s[32 + i] = __uint_as_float(r1[i]);
+                    }
+                    if (!full) {
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            s[c] = (m0 >> c) & 1u ? s[c] : -INFINITY;
+                            s[32 + c] = (m1 >> c) & 1u ? s[32 + c] : -INFINITY;
+                        }
+                    }
                 }
-            }
-            if (!full) {
-                uint32_t m[4];
-                build_row_mask(p, kc, st, m);
+                // maximum of this half row (four independent 3-input chains)
+                float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-                for (int c = 0; c < 128; ++c)
-                    s[c] = (m[c >> 5] >> (c & 31)) & 1u ? s[c] : -INFINITY;
+                for (int c = 0; c < 64; c += 8) {
+                    a0 = max3(a0, s[c], s[c + 1]);
+                    a1 = max3(a1, s[c + 2], s[c + 3]);
+                    a2 = max3(a2, s[c + 4], s[c + 5]);
+                    a3 = max3(a3, s[c + 6], s[c + 7]);
+                }
+                mx = fmaxf(max3(a0, a1, a2), a3);
             }
-            float mx = s[0];
-#pragma unroll
-            for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+            // combine with the other half of the row (always executed)
+            xchg[sb][half][row] = mx;
+            named_bar_sync(pair_bar, 64);
+            mx = fmaxf(mx, xchg[sb][half ^ 1][row]);
+            if (!ok) continue;
             const float m_tile = mx * scale_log2;   // -inf if the row is fully masked
 
             const bool need = m_tile > m_run + kTau;
@@ -438,51 +638,43 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                 m_run = m_new;
                 l_run *= alpha;
                 if (j > 0) {
-                    // O holds PV(0..j-1): wait for PV(j-1), then rescale
-                    ok = mbar_wait(bar(bars.o_done), (j - 1) & 1, &abort_flag);
-                    if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-                    tc_fence_after();
-#pragma unroll
-                    for (int c = 0; c < D; c += 32) {
-                        uint32_t r[32];
-                        tmem_ld32(tmem + kColO + lane_addr + c, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-                        tmem_st32(tmem + kColO + lane_addr + c, r);
+                    // O holds PV(0..j-1): wait for PV(j-1), then rescale this half's columns
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_done), (j - 1) & 1, &abort_flag));
+                    if (!ok) {
+                        raise_status(&abort_flag);
+                        continue;
                     }
-                    tmem_wait_st();
+                    tc_fence_after();
+                    rescale_o<C::kOHalf>(t_ohalf, alpha);
                 }
             }
             const float m_eff = (m_run == -INFINITY) ? 0.0f : m_run - kShift;
-            float rowsum = 0.0f;
+            const float2 sc2 = make_float2(scale_log2, scale_log2);
+            const float2 nm2 = make_float2(-m_eff, -m_eff);
+            float2 acc0 = make_float2(0.f, 0.f), acc1 = acc0, acc2 = acc0, acc3 = acc0;
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                s[c] = fast_exp2(fmaf(s[c], scale_log2, -m_eff));
-                rowsum += s[c];
+            for (int c = 0; c < 64; c += 8) {
+                float2 t0 = ffma2(make_float2(s[c], s[c + 1]), sc2, nm2);
+                float2 t1 = ffma2(make_float2(s[c + 2], s[c + 3]), sc2, nm2);
+                float2 t2 = ffma2(make_float2(s[c + 4], s[c + 5]), sc2, nm2);
+                float2 t3 = ffma2(make_float2(s[c + 6], s[c + 7]), sc2, nm2);
+                t0 = make_float2(fast_exp2(t0.x), fast_exp2(t0.y));
+                t1 = make_float2(fast_exp2(t1.x), fast_exp2(t1.y));
+                t2 = make_float2(fast_exp2(t2.x), fast_exp2(t2.y));
+                t3 = make_float2(fast_exp2(t3.x), fast_exp2(t3.y));
+                s[c] = t0.x; s[c + 1] = t0.y; s[c + 2] = t1.x; s[c + 3] = t1.y;
+                s[c + 4] = t2.x; s[c + 5] = t2.y; s[c + 6] = t3.x; s[c + 7] = t3.y;
+                acc0 = fadd2(acc0, t0);
+                acc1 = fadd2(acc1, t1);
+                acc2 = fadd2(acc2, t2);
+                acc3 = fadd2(acc3, t3);
             }
-            l_run += rowsum;
+            acc0 = fadd2(fadd2(acc0, acc1), fadd2(acc2, acc3));
+            l_run += acc0.x + acc0.y;
             {
-                uint32_t pk[C::kPCols];
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    float x[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) x[i] = s[c * 32 + i];
-                    pack_p<ESZ>(x, pk + c * (32 * ESZ / 4));
-                }
-                if constexpr (C::kPCols == 64) {
-                    uint32_t a[32], b[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) { a[i] = pk[i]; b[i] = pk[32 + i]; }
-                    tmem_st32(tmem + kColS0 + sb * 128 + lane_addr, a);
-                    tmem_st32(tmem + kColS0 + sb * 128 + lane_addr + 32, b);
-                } else {
-                    uint32_t a[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) a[i] = pk[i];
-                    tmem_st32(tmem + kColS0 + sb * 128 + lane_addr, a);
-                }
+                uint32_t pk[C::kPHalfWords];
+                pack_p<ESZ>(s, pk);
+                tmem_store_n<C::kPHalfWords>(t_s + half * C::kPHalfWords, pk);
                 tmem_wait_st();
             }
             tc_fence_before();
@@ -492,35 +684,37 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
 
         // ------------------------------------------------------------ epilogue
         if (ok) {
-            ok = mbar_wait(bar(bars.o_done), (n_kv - 1) & 1, &abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_done), (n_kv - 1) & 1, &abort_flag));
+            if (!ok) raise_status(&abort_flag);
         }
-        if (!ok) {
-            raise_status(&abort_flag);
-        } else {
+        // every thread of the pair reaches this exchange (even on failure)
+        xchg[n_kv & 1][half][row] = l_run;
+        named_bar_sync(pair_bar, 64);
+        const float l_tot = l_run + xchg[n_kv & 1][half ^ 1][row];
+        if (ok) {
             tc_fence_after();
-            const bool has = row_valid && l_run > 0.0f;
-            const float inv_l = has ? out_scale / l_run : 0.0f;
-            auto* out_row = reinterpret_cast<uint4*>(static_cast<uint8_t*>(p.out) +
-                                                     (q_tile_global * kTileElems + row) * static_cast<int64_t>(D) * 2);
+            const bool has = row_valid && l_tot > 0.0f;
+            const float inv_l = has ? out_scale / l_tot : 0.0f;
+            uint8_t* out_row = static_cast<uint8_t*>(p.out) + (q_tile_global * kTileElems + row) * (D * 2) + half * D;
 #pragma unroll
-            for (int c = 0; c < D; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + kColO + lane_addr + c, r);
+            for (int c = 0; c < C::kOHalf; c += 16) {
+                uint32_t r[16];
+                tmem_ld16(t_ohalf + c, r);
                 tmem_wait_ld();
-                uint32_t pk[16];
+                reg_fence(r);
+                uint32_t pk[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
+                for (int i = 0; i < 8; ++i) {
                     __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * inv_l,
                                                              __uint_as_float(r[2 * i + 1]) * inv_l);
                     pk[i] = *reinterpret_cast<uint32_t*>(&h);
                 }
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    out_row[c / 8 + v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                uint4* dst = reinterpret_cast<uint4*>(out_row + c * 2);
+                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
-            if (p.lse != nullptr) {
-                const float lse = has ? (m_run - kShift + __log2f(l_run)) * kLn2 : -INFINITY;
+            if (p.lse != nullptr && half == 0) {
+                const float lse = has ? (m_run - kShift + __log2f(l_tot)) * kLn2 : -INFINITY;
                 p.lse[q_tile_global * kTileElems + row] = lse;
             }
         }
@@ -535,17 +729,28 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     }
 }
 
-template <int D, int ESZ, int NS>
-cudaError_t launch_impl(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
+template <int D, int ESZ, int NS, int TT, int TH, int TW>
+cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
     using C = Cfg<D, ESZ, NS>;
     static_assert(NS <= 4, "barrier arrays hold 4 stages");
-    static_assert(C::kSmemAlloc <= 232448, "shared memory budget");
-    auto kern = gna_fwd_kernel<D, ESZ, NS>;
+    static_assert(C::kSmemAlloc <= 232448 - 4096, "shared memory budget");
+    static_assert(C::kQHalfWords == 8 || C::kQHalfWords == 16 || C::kQHalfWords == 32, "Q half-row width");
+    auto kern = gna_fwd_kernel<D, ESZ, NS, TT, TH, TW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     kern<<<dim3(static_cast<unsigned>(num_q_tiles)), kThreads, C::kSmemAlloc, stream>>>(p);
     return cudaGetLastError();
+}
+
+// Default tiles get a kernel with the tile shape compiled in.
+template <int D, int ESZ, int NS>
+cudaError_t launch_impl(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
+{
+    if (p.tile[0] == 2 && p.tile[1] == 8 && p.tile[2] == 8) return launch_tile<D, ESZ, NS, 2, 8, 8>(p, num_q_tiles, stream);
+    if (p.tile[0] == 1 && p.tile[1] == 8 && p.tile[2] == 16)
+        return launch_tile<D, ESZ, NS, 1, 8, 16>(p, num_q_tiles, stream);
+    return launch_tile<D, ESZ, NS, 0, 0, 0>(p, num_q_tiles, stream);
 }
 
 }  // namespace

@@ -22,7 +22,8 @@ cudaError_t launch_permute(const void* src, void* dst, const PermuteGeom& g, boo
 
 // Parameters of one attention launch (passed by value as a __grid_constant__).
 struct FwdParams {
-    CUtensorMap tmQ, tmK, tmV;   // 2-D views [rows, head_dim] of the tiled q, k, v
+    CUtensorMap tmK, tmV;        // 2-D TMA views [rows, head_dim] of the tiled k, v
+    const void* q;               // tiled q [rows, head_dim] (read row by row into TMEM)
     void* out;                   // tiled bf16 [rows, head_dim]
     float* lse;                  // tiled float [rows] or nullptr
     const float* descale;        // e4m3 only: 3 device floats (q, k, v) or nullptr
