@@ -57,6 +57,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="--impl reference: total oracle time over warm-up and timed steps")
     a = ap.parse_args(argv)
     a.dims = tuple(int(x) for x in a.dims.split(","))
     a.window = tuple(int(x) for x in a.window.split(","))
@@ -242,7 +244,7 @@ def reference_arm(a, rank, world):
     if rank != 0:
         return
     cores = os.cpu_count() or 1
-    per_step = max(1.0, 60.0 / max(1, a.steps + a.warmup))     # keep the whole run near a minute
+    per_step = a.ref_seconds / max(1, a.steps + a.warmup)     # keep the whole run near a minute
     for _ in range(a.warmup):
         oracle_rate(a, per_step, cores)
     flops = secs = 0.0
