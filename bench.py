@@ -1,7 +1,8 @@
 """Benchmark of the GNA forward hot path on B300.
 
 One step = one pass of the whole path over one batch of synthetic input:
-    permute Q, K, V (raster -> 128-token tiles)  ->  fused GNA forward
+    permute Q, K (raster -> 128-token tiles) and V (-> feature-major tiles)
+    ->  fused GNA forward
     ->  unpermute O and lse (tiles -> raster)
 on the 720p-video latent workload (30 x 48 x 80 tokens, 24 heads, head_dim 128,
 window 16 x 32 x 48, bf16), the configuration the GNA page's video results and
@@ -298,7 +299,8 @@ def gpu_arm(a, rank, world, local):
         del x
     ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)
     shp = G.tiled_shape(B, heads, dims, d)
-    qt, kt, vt = (torch.empty(shp, dtype=dt, device=dev) for _ in range(3))
+    qt, kt = (torch.empty(shp, dtype=dt, device=dev) for _ in range(2))
+    vt = torch.empty(G.value_shape(B, heads, dims, d), dtype=dt, device=dev)
     out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
     lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     out = torch.empty(raster_shape, dtype=torch.bfloat16, device=dev)
@@ -310,8 +312,9 @@ def gpu_arm(a, rank, world, local):
         if record:
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             e[0].record(stream)
-        for x, t in zip(xs, (qt, kt, vt)):
-            G.gna_permute(x, t, B, heads, dims, d, stream=stream)
+        G.gna_permute(xs[0], qt, B, heads, dims, d, stream=stream)
+        G.gna_permute(xs[1], kt, B, heads, dims, d, stream=stream)
+        G.gna_permute_v(xs[2], vt, B, heads, dims, d, stream=stream)
         if record:
             e[1].record(stream)
         G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds, stream=stream)
@@ -400,8 +403,9 @@ def gpu_arm(a, rank, world, local):
         def e2e_step():
             for h, dv in zip(host_in, dev_in):
                 dv.copy_(h, non_blocking=True)
-            for x, t in zip(dev_in, (qt, kt, vt)):
-                G.gna_permute(x, t, B, heads, dims, d, stream=stream)
+            G.gna_permute(dev_in[0], qt, B, heads, dims, d, stream=stream)
+            G.gna_permute(dev_in[1], kt, B, heads, dims, d, stream=stream)
+            G.gna_permute_v(dev_in[2], vt, B, heads, dims, d, stream=stream)
             G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds,
                           stream=stream)
             G.gna_unpermute(out_t, out, B, heads, dims, d, stream=stream)

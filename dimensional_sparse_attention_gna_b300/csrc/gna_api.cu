@@ -166,8 +166,25 @@ gna_status make_tile_map(CUtensorMap* map, const void* ptr, int64_t rows, int he
     return GNA_OK;
 }
 
+// 2-D TMA view of a tensor in the value layout: [tiles * head_dim rows, 128
+// tokens], box = head_dim rows x 128 bytes of tokens.
+gna_status make_value_map(CUtensorMap* map, const void* ptr, int64_t tiles, int head_dim, int esize)
+{
+    auto enc = encode_fn();
+    if (enc == nullptr) return fail(GNA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t gdim[2] = {static_cast<cuuint64_t>(gna::kTileElems), static_cast<cuuint64_t>(tiles * head_dim)};
+    cuuint64_t gstride[1] = {static_cast<cuuint64_t>(gna::kTileElems * esize)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), static_cast<cuuint32_t>(head_dim)};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = enc(map, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                     const_cast<void*>(ptr), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GNA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return GNA_OK;
+}
+
 gna_status permute_common(const void* src, void* dst, int B, int heads, const int dims[3], const int* tile_in,
-                          int head_dim, gna_dtype dtype, void* stream, bool to_tiled)
+                          int head_dim, gna_dtype dtype, void* stream, bool to_tiled, bool value_layout = false)
 {
     if (src == nullptr || dst == nullptr) return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
     if (!aligned16(src) || !aligned16(dst)) return fail(GNA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
@@ -195,6 +212,16 @@ gna_status permute_common(const void* src, void* dst, int B, int heads, const in
         return fail(GNA_ERR_UNSUPPORTED, "tensor too large");
     g.ntiles_total = static_cast<int>(ntiles);
     g.row_bytes = head_dim * es;
+    if (value_layout) {
+        if (es != 1 && es != 2) return fail(GNA_ERR_UNSUPPORTED, "the value layout holds 1- or 2-byte elements");
+        if (g.row_bytes % 16 != 0 || g.row_bytes > gna::kMaxValueRowBytes)
+            return fail(GNA_ERR_UNSUPPORTED, "value layout: head_dim * element size must be a multiple of 16 bytes, "
+                                             "at most %d", gna::kMaxValueRowBytes);
+        cudaError_t e = gna::launch_permute_v(src, dst, g, es, to_tiled, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, to_tiled ? "value permute launch" : "value unpermute launch");
+        t_last_error.clear();
+        return GNA_OK;
+    }
     cudaError_t e = gna::launch_permute(src, dst, g, to_tiled, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, to_tiled ? "permute launch" : "unpermute launch");
     t_last_error.clear();
@@ -262,6 +289,32 @@ gna_status gna_unpermute_tiled(const void* src, void* dst, int B, int heads, con
 {
     if (tile == nullptr) return fail(GNA_ERR_INVALID_ARG, "tile is NULL");
     return permute_common(src, dst, B, heads, dims, tile, head_dim, dtype, stream, false);
+}
+
+gna_status gna_permute_v(const void* src, void* dst, int B, int heads, const int dims[3], int head_dim,
+                         gna_dtype dtype, void* stream)
+{
+    return permute_common(src, dst, B, heads, dims, nullptr, head_dim, dtype, stream, true, true);
+}
+
+gna_status gna_unpermute_v(const void* src, void* dst, int B, int heads, const int dims[3], int head_dim,
+                           gna_dtype dtype, void* stream)
+{
+    return permute_common(src, dst, B, heads, dims, nullptr, head_dim, dtype, stream, false, true);
+}
+
+gna_status gna_permute_v_tiled(const void* src, void* dst, int B, int heads, const int dims[3], const int tile[3],
+                               int head_dim, gna_dtype dtype, void* stream)
+{
+    if (tile == nullptr) return fail(GNA_ERR_INVALID_ARG, "tile is NULL");
+    return permute_common(src, dst, B, heads, dims, tile, head_dim, dtype, stream, true, true);
+}
+
+gna_status gna_unpermute_v_tiled(const void* src, void* dst, int B, int heads, const int dims[3],
+                                 const int tile[3], int head_dim, gna_dtype dtype, void* stream)
+{
+    if (tile == nullptr) return fail(GNA_ERR_INVALID_ARG, "tile is NULL");
+    return permute_common(src, dst, B, heads, dims, tile, head_dim, dtype, stream, false, true);
 }
 
 gna_status gna_tile_stats(const int dims[3], const int window[3], const int stride[3], const int tile_in[3],
@@ -348,7 +401,7 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out
 
     p.q = q;
     if ((st = make_tile_map(&p.tmK, k, rows, head_dim, es)) != GNA_OK) return st;
-    if ((st = make_tile_map(&p.tmV, v, rows, head_dim, es)) != GNA_OK) return st;
+    if ((st = make_value_map(&p.tmV, v, num_q_tiles, head_dim, es)) != GNA_OK) return st;
 
     cudaError_t e = gna::launch_forward(p, head_dim, es, num_q_tiles, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(GNA_ERR_UNSUPPORTED, "no kernel for head_dim %d", head_dim);

@@ -22,7 +22,9 @@
 // TMEM (512 columns): O [0, 128), S double buffer [128, 256) and [256, 384),
 // Q [384, 384 + head_dim * elem / 4).  Q sits in TMEM so S = Q K^T reads only
 // K from shared memory; P overwrites the front of its S buffer (bf16: 64
-// columns, e4m3: 32) and feeds O += P V straight from TMEM.
+// columns, e4m3: 32) and feeds O += P V straight from TMEM.  V comes in the
+// value layout (each tile feature-major), so both MMAs read their shared-memory
+// operand K-major.
 // MMA issue order  QK(0) QK(1) PV(0) QK(2) PV(1) ...  keeps the tensor core on
 // the next S while the softmax warps work on the current one.
 //
@@ -93,7 +95,12 @@ struct Cfg {
     static constexpr int kQKSteps = kRowBytesAll / 32;
     static constexpr int kPVSteps = kTileElems / kKPerInstr;
     static constexpr uint32_t kIdescQK = make_idesc(128, 128, Precision<ESZ>::fmt, false);
-    static constexpr uint32_t kIdescPV = make_idesc(128, D, Precision<ESZ>::fmt, true);
+    static constexpr uint32_t kIdescPV = make_idesc(128, D, Precision<ESZ>::fmt, false);
+    // V arrives in the value layout: a d x 128 (feature-major) tile, loaded as
+    // ESZ boxes of d rows x 128 bytes, which is the K-major B operand of P V
+    static constexpr int kVChunks = ESZ;
+    static constexpr int kVChunkBytes = D * 128;
+    static constexpr int kVChunkElems = 128 / ESZ;
     static constexpr int kQHalfWords = kRowBytesAll / 8;                     // TMEM columns of half a Q row
     static constexpr int kPHalfWords = 64 * ESZ / 4;                         // TMEM columns of half a P row
     static constexpr int kOHalf = D / 2;                                     // O columns per half
@@ -390,10 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             }
             if (elect_one_sync()) {
                 mbar_arrive_expect_tx(bar(bars.v_full[s]), C::kTileBytes);
+                const int32_t vrow = static_cast<int32_t>((kv_row_base / kTileElems + tile_id) * D);
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_2d(sV + s * C::kTileBytes + c * kTileElems * C::kRowBytes, &p.tmV, bar(bars.v_full[s]),
-                                c * C::kChunkElems, row);
+                for (int c = 0; c < C::kVChunks; ++c)
+                    tma_load_2d(sV + s * C::kTileBytes + c * C::kVChunkBytes, &p.tmV, bar(bars.v_full[s]),
+                                c * C::kVChunkElems, vrow);
             }
             __syncwarp();
             ++v_issued;
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         // descriptors of stage 0, chunk 0; stage / k-step offsets are added
         // to the start-address field (addresses >> 4 stay below 2^14)
         const uint64_t dK0 = make_smem_desc(sK, 16, 8 * C::kRowBytes, C::kSwizzle);
-        const uint64_t dV0 = make_smem_desc(sV, kTileElems * C::kRowBytes, 8 * C::kRowBytes, C::kSwizzle);
+        const uint64_t dV0 = make_smem_desc(sV, 16, 1024, kSwizzle128B);
         auto issue_pv = [&](int i) -> bool {
             const int s = i % NS;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.v_full[s]), (i / NS) & 1, &abort_flag))) return false;
@@ -426,7 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                 const uint32_t tP = tmem + kColS0 + (i & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < C::kPVSteps; ++kk) {
-                    const uint64_t d = dv + static_cast<uint64_t>((kk * C::kKPerInstr * C::kRowBytes) >> 4);
+                    // k-step kk covers tokens [kk * K, kk * K + K): 32 bytes of every feature row
+                    const int off = ((kk * 32) / 128) * C::kVChunkBytes + ((kk * 32) % 128);
+                    const uint64_t d = dv + static_cast<uint64_t>(off >> 4);
                     if (ESZ == 2) mma_f16_ts(tO, tP + kk * 8, d, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                     else mma_f8_ts(tO, tP + kk * 8, d, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                 }

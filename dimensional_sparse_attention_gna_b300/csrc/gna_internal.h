@@ -20,9 +20,17 @@ struct PermuteGeom {
 
 cudaError_t launch_permute(const void* src, void* dst, const PermuteGeom& g, bool to_tiled, cudaStream_t stream);
 
+// Raster <-> value layout (each tile stored feature-major, d x 128).  Element
+// size 1 or 2 bytes, row_bytes a multiple of 16 and at most kMaxValueRowBytes;
+// returns cudaErrorNotSupported otherwise.
+constexpr int kMaxValueRowBytes = 256;
+cudaError_t launch_permute_v(const void* src, void* dst, const PermuteGeom& g, int elem_size, bool to_tiled,
+                             cudaStream_t stream);
+
 // Parameters of one attention launch (passed by value as a __grid_constant__).
 struct FwdParams {
-    CUtensorMap tmK, tmV;        // 2-D TMA views [rows, head_dim] of the tiled k, v
+    CUtensorMap tmK;             // 2-D TMA view [rows, head_dim] of the tiled k
+    CUtensorMap tmV;             // 2-D TMA view [rows * head_dim / 128, 128] of v in the value layout
     const void* q;               // tiled q [rows, head_dim] (read row by row into TMEM)
     void* out;                   // tiled bf16 [rows, head_dim]
     float* lse;                  // tiled float [rows] or nullptr

@@ -17,6 +17,12 @@
 // sequence of whole rows.  The raster offset of each row is computed once per
 // CTA into shared memory (-1 for padding rows, which read as zero and are
 // skipped on the way back).
+//
+// The value layout [B, heads, nT, nH, nW, d, tT*tH*tW] stores each tile
+// feature-major (its d x 128 transpose), so that the attention kernel's P V
+// product reads V with the token index contiguous, the operand order the
+// tensor core consumes fastest.  permute_v_kernel stages one tile in shared
+// memory and transposes it in registers with byte permutes.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -35,14 +41,10 @@ template <> struct VecT<16> { using type = uint4; };
 template <> struct VecT<8> { using type = uint2; };
 template <> struct VecT<4> { using type = uint32_t; };
 
-template <int VEC, bool TO_TILED>
-__global__ void __launch_bounds__(kPermThreads)
-permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, PermuteGeom g)
+// Raster byte offset of every element of tile `tile_global` ((b*heads + h)*ntiles
+// + tile), or -1 for padding, into row_off[0..127].  Ends with __syncthreads().
+__device__ __forceinline__ void tile_row_offsets(const PermuteGeom& g, int64_t tile_global, int64_t* row_off)
 {
-    using V = typename VecT<VEC>::type;
-    __shared__ int64_t row_off[kTileElems];
-
-    const int64_t tile_global = blockIdx.x;                   // (b*heads + h)*ntiles + tile
     const int tile_id = static_cast<int>(tile_global % g.ntiles_total);
     const int64_t bh = tile_global / g.ntiles_total;
     const int h = static_cast<int>(bh % g.heads);
@@ -51,7 +53,7 @@ permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Permu
     const int ty = (tile_id / g.nt[2]) % g.nt[1];
     const int tt = tile_id / (g.nt[2] * g.nt[1]);
 
-    for (int e = threadIdx.x; e < kTileElems; e += kPermThreads) {
+    for (int e = threadIdx.x; e < kTileElems; e += blockDim.x) {
         const int ix = e & ((1 << g.tlog[2]) - 1);
         const int iy = (e >> g.tlog[2]) & ((1 << g.tlog[1]) - 1);
         const int it = e >> (g.tlog[1] + g.tlog[2]);
@@ -64,6 +66,17 @@ permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Permu
         row_off[e] = off;
     }
     __syncthreads();
+}
+
+template <int VEC, bool TO_TILED>
+__global__ void __launch_bounds__(kPermThreads)
+permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, PermuteGeom g)
+{
+    using V = typename VecT<VEC>::type;
+    __shared__ int64_t row_off[kTileElems];
+
+    const int64_t tile_global = blockIdx.x;                   // (b*heads + h)*ntiles + tile
+    tile_row_offsets(g, tile_global, row_off);
 
     const int vpr = g.row_bytes / VEC;                        // vectors per row
     const int nvec = kTileElems * vpr;
@@ -106,6 +119,142 @@ permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Permu
     }
 }
 
+// Raster <-> value layout for elements of E bytes (E = 1 or 2; rows of a
+// multiple of 16 bytes, at most 256).  Shared memory holds the tile token-major,
+// [128 tokens][W words + 4 pad] (W = d*E/4), 16-byte aligned rows.
+// Transposed side: thread (word column c, group of 16 tokens) owns the 4/E
+// feature rows of column c for those 16 tokens: 16*E contiguous bytes each.
+// With consecutive lanes on consecutive columns every shared-memory access of
+// a warp is conflict-free.
+template <int E>
+__device__ __forceinline__ void words_to_feature_rows(const uint32_t (&w)[16], uint4 (&rows)[4 / E][E])
+{
+    if constexpr (E == 2) {
+        uint32_t lo[8], hi[8];                       // feature 2c / 2c+1 of tokens 2i, 2i+1
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            lo[i] = __byte_perm(w[2 * i], w[2 * i + 1], 0x5410);
+            hi[i] = __byte_perm(w[2 * i], w[2 * i + 1], 0x7632);
+        }
+        rows[0][0] = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        rows[0][1] = make_uint4(lo[4], lo[5], lo[6], lo[7]);
+        rows[1][0] = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        rows[1][1] = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+    } else {
+        uint32_t r[4][4];                            // [feature byte][group of 4 tokens]
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            // 4 x 4 byte transpose of words w[4q..4q+3]
+            const uint32_t a = __byte_perm(w[4 * q], w[4 * q + 1], 0x5140);
+            const uint32_t b = __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x5140);
+            const uint32_t c = __byte_perm(w[4 * q], w[4 * q + 1], 0x7362);
+            const uint32_t d = __byte_perm(w[4 * q + 2], w[4 * q + 3], 0x7362);
+            r[0][q] = __byte_perm(a, b, 0x5410);
+            r[1][q] = __byte_perm(a, b, 0x7632);
+            r[2][q] = __byte_perm(c, d, 0x5410);
+            r[3][q] = __byte_perm(c, d, 0x7632);
+        }
+#pragma unroll
+        for (int f = 0; f < 4; ++f) rows[f][0] = make_uint4(r[f][0], r[f][1], r[f][2], r[f][3]);
+    }
+}
+
+// Inverse of words_to_feature_rows (both byte networks are involutions up to
+// the grouping of their inputs).
+template <int E>
+__device__ __forceinline__ void feature_rows_to_words(const uint4 (&rows)[4 / E][E], uint32_t (&w)[16])
+{
+    if constexpr (E == 2) {
+        const uint32_t lo[8] = {rows[0][0].x, rows[0][0].y, rows[0][0].z, rows[0][0].w,
+                                rows[0][1].x, rows[0][1].y, rows[0][1].z, rows[0][1].w};
+        const uint32_t hi[8] = {rows[1][0].x, rows[1][0].y, rows[1][0].z, rows[1][0].w,
+                                rows[1][1].x, rows[1][1].y, rows[1][1].z, rows[1][1].w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            w[2 * i] = __byte_perm(lo[i], hi[i], 0x5410);
+            w[2 * i + 1] = __byte_perm(lo[i], hi[i], 0x7632);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t r0 = (&rows[0][0].x)[q], r1 = (&rows[1][0].x)[q];
+            const uint32_t r2 = (&rows[2][0].x)[q], r3 = (&rows[3][0].x)[q];
+            const uint32_t a = __byte_perm(r0, r1, 0x5140);
+            const uint32_t b = __byte_perm(r2, r3, 0x5140);
+            const uint32_t c = __byte_perm(r0, r1, 0x7362);
+            const uint32_t d = __byte_perm(r2, r3, 0x7362);
+            w[4 * q] = __byte_perm(a, b, 0x5410);
+            w[4 * q + 1] = __byte_perm(a, b, 0x7632);
+            w[4 * q + 2] = __byte_perm(c, d, 0x5410);
+            w[4 * q + 3] = __byte_perm(c, d, 0x7632);
+        }
+    }
+}
+
+template <int E, bool TO_TILED>
+__global__ void __launch_bounds__(kPermThreads)
+permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, PermuteGeom g)
+{
+    constexpr int F = 4 / E;                                  // features per 32-bit word
+    extern __shared__ __align__(16) uint32_t vsm[];
+    __shared__ int64_t row_off[kTileElems];
+
+    const int64_t tile_global = blockIdx.x;
+    tile_row_offsets(g, tile_global, row_off);
+
+    const int W = g.row_bytes / 4;                            // words per token row
+    const int S = W + 4;                                      // padded row stride (words)
+    const int vpr = g.row_bytes / 16;                         // 16-byte vectors per token row
+    const int64_t tile_base = tile_global * kTileElems * static_cast<int64_t>(g.row_bytes);
+    const int frow = kTileElems * E;                          // bytes of one feature row
+
+    if (TO_TILED) {
+        for (int i = threadIdx.x; i < kTileElems * vpr; i += kPermThreads) {
+            const int r = i / vpr, v = i - r * vpr;
+            const int64_t o = row_off[r];
+            const uint4 val = o >= 0 ? *reinterpret_cast<const uint4*>(src + o + v * 16) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vsm + r * S + v * 4) = val;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < W * 8; i += kPermThreads) {
+            const int c = i % W, grp = i / W;
+            uint32_t w[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) w[k] = vsm[(grp * 16 + k) * S + c];
+            uint4 rows[F][E];
+            words_to_feature_rows<E>(w, rows);
+#pragma unroll
+            for (int f = 0; f < F; ++f) {
+                uint4* o = reinterpret_cast<uint4*>(dst + tile_base + static_cast<int64_t>(c * F + f) * frow + grp * 16 * E);
+#pragma unroll
+                for (int e = 0; e < E; ++e) o[e] = rows[f][e];
+            }
+        }
+    } else {
+        for (int i = threadIdx.x; i < W * 8; i += kPermThreads) {
+            const int c = i % W, grp = i / W;
+            uint4 rows[F][E];
+#pragma unroll
+            for (int f = 0; f < F; ++f) {
+                const uint4* o =
+                    reinterpret_cast<const uint4*>(src + tile_base + static_cast<int64_t>(c * F + f) * frow + grp * 16 * E);
+#pragma unroll
+                for (int e = 0; e < E; ++e) rows[f][e] = o[e];
+            }
+            uint32_t w[16];
+            feature_rows_to_words<E>(rows, w);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) vsm[(grp * 16 + k) * S + c] = w[k];
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < kTileElems * vpr; i += kPermThreads) {
+            const int r = i / vpr, v = i - r * vpr;
+            const int64_t o = row_off[r];
+            if (o >= 0) *reinterpret_cast<uint4*>(dst + o + v * 16) = *reinterpret_cast<const uint4*>(vsm + r * S + v * 4);
+        }
+    }
+}
+
 template <bool TO_TILED>
 cudaError_t launch(const void* src, void* dst, const PermuteGeom& g, cudaStream_t stream)
 {
@@ -128,6 +277,27 @@ cudaError_t launch(const void* src, void* dst, const PermuteGeom& g, cudaStream_
 cudaError_t launch_permute(const void* src, void* dst, const PermuteGeom& g, bool to_tiled, cudaStream_t stream)
 {
     return to_tiled ? launch<true>(src, dst, g, stream) : launch<false>(src, dst, g, stream);
+}
+
+cudaError_t launch_permute_v(const void* src, void* dst, const PermuteGeom& g, int elem_size, bool to_tiled,
+                             cudaStream_t stream)
+{
+    const int64_t nblocks = g.B * static_cast<int64_t>(g.heads) * g.ntiles_total;
+    if (nblocks <= 0) return cudaSuccess;
+    if (g.row_bytes % 16 != 0 || g.row_bytes > kMaxValueRowBytes || (elem_size != 1 && elem_size != 2))
+        return cudaErrorNotSupported;
+    const size_t smem = static_cast<size_t>(kTileElems) * (g.row_bytes / 4 + 4) * sizeof(uint32_t);
+    dim3 grid(static_cast<unsigned>(nblocks));
+    const auto* s = static_cast<const uint8_t*>(src);
+    auto* d = static_cast<uint8_t*>(dst);
+    if (elem_size == 2) {
+        if (to_tiled) permute_v_kernel<2, true><<<grid, kPermThreads, smem, stream>>>(s, d, g);
+        else permute_v_kernel<2, false><<<grid, kPermThreads, smem, stream>>>(s, d, g);
+    } else {
+        if (to_tiled) permute_v_kernel<1, true><<<grid, kPermThreads, smem, stream>>>(s, d, g);
+        else permute_v_kernel<1, false><<<grid, kPermThreads, smem, stream>>>(s, d, g);
+    }
+    return cudaGetLastError();
 }
 
 }  // namespace gna

@@ -78,7 +78,11 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = st
             f.argtypes = [_P, _P, _INT, _INT, _I3, _INT, _INT, _P]
-        for name in ("gna_permute_tiled", "gna_unpermute_tiled"):
+        for name in ("gna_permute_v", "gna_unpermute_v"):
+            f = getattr(L, name)
+            f.restype = st
+            f.argtypes = [_P, _P, _INT, _INT, _I3, _INT, _INT, _P]
+        for name in ("gna_permute_tiled", "gna_unpermute_tiled", "gna_permute_v_tiled", "gna_unpermute_v_tiled"):
             f = getattr(L, name)
             f.restype = st
             f.argtypes = [_P, _P, _INT, _INT, _I3, _I3, _INT, _INT, _P]
@@ -178,13 +182,48 @@ def gna_unpermute(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims
     _check(st)
 
 
+def value_shape(B: int, heads: int, dims, head_dim: int, tile=None) -> tuple[int, ...]:
+    """Shape ``[B, heads, tiles, head_dim, 128]`` of a tensor in the value layout."""
+    s = tiled_shape(B, heads, dims, head_dim, tile)
+    return (B, heads, s[2], head_dim, TILE_ELEMS)
+
+
+def gna_permute_v(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims, head_dim: int,
+                  tile=None, stream=None):
+    """Raster ``[B, T, H, W, heads, d]`` -> value layout ``[B, heads, tiles, d, 128]`` (zero padding)."""
+    code = dtype_code(src.dtype)
+    if dst.dtype != src.dtype:
+        raise ValueError("src and dst dtypes differ")
+    if tile is None:
+        st = lib().gna_permute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+    else:
+        st = lib().gna_permute_v_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
+                                       _stream_ptr(stream))
+    _check(st)
+
+
+def gna_unpermute_v(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims, head_dim: int,
+                    tile=None, stream=None):
+    """Value layout ``[B, heads, tiles, d, 128]`` -> raster ``[B, T, H, W, heads, d]``."""
+    code = dtype_code(src.dtype)
+    if dst.dtype != src.dtype:
+        raise ValueError("src and dst dtypes differ")
+    if tile is None:
+        st = lib().gna_unpermute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+    else:
+        st = lib().gna_unpermute_v_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
+                                         _stream_ptr(stream))
+    _check(st)
+
+
 def gna_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None,
                 B: int, heads: int, dims, window, stride, head_dim: int, *, tile=None,
                 leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, descale: torch.Tensor | None = None,
                 stream=None):
     """GNA forward on tiled tensors (see ``include/gna.h``).
 
-    ``q, k, v``: bf16 or float8_e4m3fn, tiled; ``out``: bf16 tiled; ``lse``:
+    ``q, k``: bf16 or float8_e4m3fn, tiled; ``v``: same dtype, value layout
+    (:func:`gna_permute_v`); ``out``: bf16 tiled; ``lse``:
     float32 ``[B, heads, tiles, 128]`` or None; ``descale``: float32 device
     tensor of 3 values (e4m3 only) or None.
     """

@@ -34,10 +34,16 @@
  *          two (GNA page §1.1: Q and KV are split into fixed-size
  *          multi-dimensional tiles; §2.2: tokens are permuted into this order
  *          before attention and back after it).
- * gna_forward reads and writes the tiled layout; gna_permute / gna_unpermute
- * convert.  lse is tiled like a d = 1 float tensor: [B, heads, tiles, 128],
- * and gna_unpermute(head_dim = 1, GNA_F32) turns it into raster
- * [B, T, H, W, heads].
+ * value  : [B, heads, nT, nH, nW, d, tT*tH*tW]
+ *          the tiled layout with every tile stored transposed (feature-major:
+ *          row f of a tile holds feature f of its 128 tokens).  gna_forward
+ *          reads v in this layout: P V then streams V with the token index
+ *          contiguous, the operand order the tensor core reads fastest.
+ * gna_forward reads q and k in the tiled layout, v in the value layout, and
+ * writes out tiled; gna_permute / gna_unpermute and gna_permute_v /
+ * gna_unpermute_v convert.  lse is tiled like a d = 1 float tensor:
+ * [B, heads, tiles, 128], and gna_unpermute(head_dim = 1, GNA_F32) turns it
+ * into raster [B, T, H, W, heads].
  *
  * Conventions
  * -----------
@@ -122,12 +128,29 @@ gna_status gna_permute_tiled(const void* src, void* dst, int B, int heads, const
 gna_status gna_unpermute_tiled(const void* src, void* dst, int B, int heads, const int dims[3],
                                const int tile[3], int head_dim, gna_dtype dtype, void* stream);
 
+/* Raster -> value layout (zero padding) and back (padding dropped): the
+ * tiled layout with each tile transposed to d x 128.  Same element count as
+ * the tiled layout (gna_tiled_elems).  dtype GNA_BF16 or GNA_FP8_E4M3 with
+ * head_dim * element size a multiple of 16 bytes and at most 256 bytes
+ * (otherwise GNA_ERR_UNSUPPORTED); src and dst must not overlap.  GNA page
+ * §2.2 (the permutation is a dedicated copy kernel; here it also produces the
+ * operand order of the P V product). */
+gna_status gna_permute_v(const void* src, void* dst, int B, int heads, const int dims[3],
+                         int head_dim, gna_dtype dtype, void* stream);
+gna_status gna_unpermute_v(const void* src, void* dst, int B, int heads, const int dims[3],
+                           int head_dim, gna_dtype dtype, void* stream);
+gna_status gna_permute_v_tiled(const void* src, void* dst, int B, int heads, const int dims[3],
+                               const int tile[3], int head_dim, gna_dtype dtype, void* stream);
+gna_status gna_unpermute_v_tiled(const void* src, void* dst, int B, int heads, const int dims[3],
+                                 const int tile[3], int head_dim, gna_dtype dtype, void* stream);
+
 /* ------------------------------------------------------------ forward ---- */
 
 /* GNA forward pass (GNA page §1.1 window rule, §2.1 kernel structure).
  *
- * q, k, v : tiled [B, heads, tiles, 128, head_dim], dtype GNA_BF16 or
- *           GNA_FP8_E4M3 (all three the same)
+ * q, k    : tiled [B, heads, tiles, 128, head_dim] (gna_permute)
+ * v       : value layout [B, heads, tiles, head_dim, 128] (gna_permute_v)
+ *           q, k, v all GNA_BF16 or all GNA_FP8_E4M3
  * out     : tiled [B, heads, tiles, 128, head_dim] bfloat16 (also for fp8
  *           inputs); padding rows are written as zero
  * lse     : tiled [B, heads, tiles, 128] float32, natural log; may be NULL

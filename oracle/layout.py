@@ -12,7 +12,8 @@ chosen here makes each multi-dimensional tile a contiguous run of rows:
 
 Inside a tile the element index is ``(it * tH + iy) * tW + ix``.  Grid
 positions past the end of a dimension (the padding of the last tile) hold
-zeros.  The per-token ``lse`` uses the same mapping with ``d = 1``.
+zeros.  The per-token ``lse`` uses the same mapping with ``d = 1``.  The value
+layout stores every tile of the tiled layout transposed, ``[.., d, 128]``.
 """
 from __future__ import annotations
 
@@ -46,6 +47,12 @@ def unpermute_reference(y: np.ndarray, dims, tile) -> np.ndarray:
     z = z.transpose(0, 2, 5, 3, 6, 4, 7, 1, 8)
     z = np.ascontiguousarray(z).reshape(B, nT * tT, nH * tH, nW * tW, heads, d)
     return np.ascontiguousarray(z[:, :T, :H, :W])
+
+
+def permute_v_reference(x: np.ndarray, tile) -> np.ndarray:
+    """Raster -> value layout ``[B, heads, nT, nH, nW, d, tT*tH*tW]``: every tile of
+    :func:`permute_reference` transposed to feature-major."""
+    return np.ascontiguousarray(np.swapaxes(permute_reference(x, tile), -1, -2))
 
 
 def tiled_row(b, h, t, y, x, heads, dims, tile) -> int:

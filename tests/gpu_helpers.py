@@ -26,14 +26,17 @@ def gpu_gna(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dims, window, str
             leader_rule=G.GNA_LEADER_CENTER, scale=0.0, descale=None):
     """Raster CPU tensors [B, T, H, W, heads, d] -> (out raster float32 [.., d], lse raster [.., heads]).
 
-    Uploads, permutes, runs the forward, unpermutes out and lse, downloads.
+    Uploads, permutes (q, k tiled; v into the value layout), runs the forward,
+    unpermutes out and lse, downloads.
     """
     B, T, H, W, heads, d = q.shape
     dev = torch.device("cuda")
     shp = G.tiled_shape(B, heads, dims, d, tile)
-    qt, kt, vt = (torch.empty(shp, dtype=x.dtype, device=dev) for x in (q, k, v))
-    for src, dst in ((q, qt), (k, kt), (v, vt)):
+    qt, kt = (torch.empty(shp, dtype=x.dtype, device=dev) for x in (q, k))
+    vt = torch.empty(G.value_shape(B, heads, dims, d, tile), dtype=v.dtype, device=dev)
+    for src, dst in ((q, qt), (k, kt)):
         G.gna_permute(src.to(dev).contiguous(), dst, B, heads, dims, d, tile=tile)
+    G.gna_permute_v(v.to(dev).contiguous(), vt, B, heads, dims, d, tile=tile)
     out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
     lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)

@@ -1,4 +1,5 @@
-"""gna_permute / gna_unpermute against the layout definition: bit-exact."""
+"""gna_permute / gna_unpermute and gna_permute_v / gna_unpermute_v against the
+layout definitions: bit-exact."""
 import numpy as np
 import pytest
 import torch
@@ -73,3 +74,57 @@ def test_permute_full_size_round_trip_and_samples(B, heads, dims, dtype):
 def _bits_gpu(t):
     view = {1: torch.uint8, 2: torch.int16, 4: torch.int32}[t.element_size()]
     return t.view(view)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float8_e4m3fn])
+@pytest.mark.parametrize("B,heads,dims,d,tile", [
+    (1, 2, (1, 16, 16), 32, None),
+    (2, 3, (3, 5, 7), 64, None),             # every tile padded
+    (1, 4, (5, 24, 40), 128, (1, 8, 16)),
+    (2, 1, (6, 20, 24), 128, (2, 4, 16)),
+    (1, 2, (2, 40, 40), 16, (1, 1, 128)),
+    (1, 1, (2, 16, 16), 256, None),          # 256-byte feature rows at 1 byte
+])
+def test_value_permute_matches_layout_definition(dtype, B, heads, dims, d, tile):
+    esz = torch.tensor([], dtype=dtype).element_size()
+    if (d * esz) % 16 or d * esz > 256:
+        pytest.skip("value layout rows are a multiple of 16 bytes, at most 256")
+    x = torch.from_numpy(normal_raster(8, B, dims, heads, d)).to(dtype)
+    t = tile or G.gna_tile_shape(dims)
+    want = layout.permute_v_reference(_bits(x), t)
+    xd = x.cuda()
+    shape = G.value_shape(B, heads, dims, d, tile)
+    nbytes = int(np.prod(shape)) * x.element_size()
+    y = torch.full((nbytes,), 0x55, dtype=torch.uint8, device="cuda").view(dtype).reshape(shape)   # poison
+    G.gna_permute_v(xd, y, B, heads, dims, d, tile=tile)
+    got = _bits(y).reshape(want.shape)
+    np.testing.assert_array_equal(got, want)
+    back = torch.zeros_like(xd)
+    G.gna_unpermute_v(y, back, B, heads, dims, d, tile=tile)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(_bits(back), _bits(x))
+
+
+@pytest.mark.parametrize("B,heads,dims,dtype", [
+    (1, 24, (30, 48, 80), torch.bfloat16),
+    (2, 24, (30, 48, 80), torch.float8_e4m3fn),
+])
+def test_value_permute_full_size_round_trip_and_samples(B, heads, dims, dtype):
+    d = 128
+    gen = torch.Generator(device="cuda").manual_seed(12)
+    x = torch.randn((B,) + dims + (heads, d), device="cuda", generator=gen).to(dtype)
+    y = torch.empty(G.value_shape(B, heads, dims, d), dtype=dtype, device="cuda")
+    G.gna_permute_v(x, y, B, heads, dims, d)
+    back = torch.empty_like(x)
+    G.gna_unpermute_v(y, back, B, heads, dims, d)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits_gpu(back), _bits_gpu(x))
+    # sampled tokens: feature column of the token's tile equals the raster row
+    tile = G.gna_tile_shape(dims)
+    rng = np.random.default_rng(4)
+    yt = y.reshape(-1, d, 128)
+    for _ in range(256):
+        b, h = int(rng.integers(B)), int(rng.integers(heads))
+        t, yy, xx = (int(rng.integers(L)) for L in dims)
+        r = layout.tiled_row(b, h, t, yy, xx, heads, dims, tile)
+        assert torch.equal(_bits_gpu(yt[r // 128, :, r % 128].contiguous()), _bits_gpu(x[b, t, yy, xx, h]))

@@ -300,6 +300,21 @@ def test_layout_hand_example():
     assert y[0, 0, 0, 0, :, :, 0].tolist() == [[0, 1, 4, 5], [2, 3, 6, 7]]
 
 
+def test_value_layout_is_the_tile_transposed():
+    """Value layout: feature f of token e of a tile sits at [.., f, e]; hand example
+    on a 1 x 2 x 4 grid with tile (1, 2, 2), one head, d = 3."""
+    x = np.arange(1 * 1 * 2 * 4 * 1 * 3).reshape(1, 1, 2, 4, 1, 3)
+    y = layout.permute_v_reference(x, (1, 2, 2))
+    assert y.shape == (1, 1, 1, 1, 2, 3, 4)
+    # tile 0 holds x = 0, 1 of both rows: tokens (y, x) = (0,0), (0,1), (1,0), (1,1)
+    tok = [(0, 0), (0, 1), (1, 0), (1, 1)]
+    for e, (yy, xx) in enumerate(tok):
+        for f in range(3):
+            assert y[0, 0, 0, 0, 0, f, e] == x[0, 0, yy, xx, 0, f]
+            assert y[0, 0, 0, 0, 1, f, e] == x[0, 0, yy, xx + 2, 0, f]
+    np.testing.assert_array_equal(np.swapaxes(y, -1, -2), layout.permute_reference(x, (1, 2, 2)))
+
+
 def test_layout_padding_and_round_trip():
     """Ragged dims: padding positions are zero; unpermute inverts permute exactly."""
     dims, tile = (3, 5, 7), (2, 4, 4)
