@@ -365,11 +365,13 @@ def gpu_arm(a, rank, world, local):
     unperm_bytes = 2 * B * math.prod(dims) * heads * (d * 2 + 4)
 
     peaks, peaks_kind = load_peaks()
-    pk = "bf16_tflops_sustained" if a.dtype == "bf16" else "bf16_tflops_sustained"
-    peak = peaks.get(pk, FALLBACK_PEAKS["bf16_tflops_sustained"])
-    if a.dtype == "fp8":
-        peak *= 2.0     # fp8 dense rate is twice bf16 (nominal 4.5 vs 2.25 PFLOP/s)
-    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * (2.0 if a.dtype == "fp8" else 1.0)
+    # Denominators: the measured cuBLAS bf16 GEMM rates (fp8 takes twice the
+    # bf16 rate, the nominal 4.5 / 2.25 PFLOP/s ratio).  The timed region is
+    # well under a second, before the board reaches its average power cap, so
+    # the burst figure is the matching one; the sustained one is reported too.
+    mult = 2.0 if a.dtype == "fp8" else 1.0
+    peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * mult
+    peak_sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * mult
 
     # tile-level work of the launch (what the tensor cores execute)
     visited, partial, nq = G.gna_tile_stats(dims, a.window, a.stride)
@@ -455,10 +457,10 @@ def gpu_arm(a, rank, world, local):
                    "l2": "inputs larger than L2 (3 x %.0f MB raster + tiled copies)" % (
                        B * math.prod(dims) * heads * d * esz / 1e6),
                    "parallelism": f"replicas x{world}: every rank runs the full workload on its own data"},
-        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
-                     "frac": kernel_tflops / peak, "traffic": traffic,
-                     "peak_source": f"{peaks_kind} {'bf16' if a.dtype == 'bf16' else 'fp8 (2x bf16)'} sustained",
-                     "frac_of_burst_peak": kernel_tflops / peak_burst,
+        "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_burst, "unit": "TFLOP/s",
+                     "frac": kernel_tflops / peak_burst, "traffic": traffic,
+                     "peak_source": f"{peaks_kind} {'bf16' if a.dtype == 'bf16' else 'fp8 (2x bf16)'} burst",
+                     "frac_of_sustained_peak": kernel_tflops / peak_sustained,
                      "tile_work_tflops": tile_flops / (fwd_ms / 1e3) / 1e12,
                      "tile_overhead": tile_flops / flops_rank, "partial_tile_share": partial / visited},
         "kernels_ms": {"permute_qkv": perm_ms, "forward": fwd_ms, "unpermute_o_lse": unperm_ms},

@@ -214,9 +214,9 @@ gna_status permute_common(const void* src, void* dst, int B, int heads, const in
     g.row_bytes = head_dim * es;
     if (value_layout) {
         if (es != 1 && es != 2) return fail(GNA_ERR_UNSUPPORTED, "the value layout holds 1- or 2-byte elements");
-        if (g.row_bytes % 16 != 0 || g.row_bytes > gna::kMaxValueRowBytes)
-            return fail(GNA_ERR_UNSUPPORTED, "value layout: head_dim * element size must be a multiple of 16 bytes, "
-                                             "at most %d", gna::kMaxValueRowBytes);
+        if (g.row_bytes < 16 || g.row_bytes > gna::kMaxValueRowBytes || (g.row_bytes & (g.row_bytes - 1)) != 0)
+            return fail(GNA_ERR_UNSUPPORTED, "value layout: head_dim * element size must be a power of two "
+                                             "from 16 to %d bytes", gna::kMaxValueRowBytes);
         cudaError_t e = gna::launch_permute_v(src, dst, g, es, to_tiled, static_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) return cuda_fail(e, to_tiled ? "value permute launch" : "value unpermute launch");
         t_last_error.clear();

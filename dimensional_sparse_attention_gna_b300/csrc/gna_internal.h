@@ -21,7 +21,7 @@ struct PermuteGeom {
 cudaError_t launch_permute(const void* src, void* dst, const PermuteGeom& g, bool to_tiled, cudaStream_t stream);
 
 // Raster <-> value layout (each tile stored feature-major, d x 128).  Element
-// size 1 or 2 bytes, row_bytes a multiple of 16 and at most kMaxValueRowBytes;
+// size 1 or 2 bytes, row_bytes a power of two from 16 to kMaxValueRowBytes;
 // returns cudaErrorNotSupported otherwise.
 constexpr int kMaxValueRowBytes = 256;
 cudaError_t launch_permute_v(const void* src, void* dst, const PermuteGeom& g, int elem_size, bool to_tiled,

@@ -120,12 +120,14 @@ permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Permu
 }
 
 // Raster <-> value layout for elements of E bytes (E = 1 or 2; rows of a
-// multiple of 16 bytes, at most 256).  Shared memory holds the tile token-major,
-// [128 tokens][W words + 4 pad] (W = d*E/4), 16-byte aligned rows.
-// Transposed side: thread (word column c, group of 16 tokens) owns the 4/E
-// feature rows of column c for those 16 tokens: 16*E contiguous bytes each.
-// With consecutive lanes on consecutive columns every shared-memory access of
-// a warp is conflict-free.
+// power of two from 16 to 256 bytes).  Shared memory holds the tile token-major,
+// [128 tokens][W words] (W = d*E/4), with the 16-byte groups of token r stored
+// at group index (group ^ (r / 16) mod (W / 4)).  On the transposed side a
+// thread owns word column c (features 4/E*c ..) of a group of 16 tokens: 16*E
+// contiguous bytes of each of its 4/E feature rows.  Eight consecutive lanes
+// take the eight token groups of one column, so a warp writes (or reads) whole
+// 128*E-byte feature rows, and the XOR spreads those eight lanes over distinct
+// banks.
 template <int E>
 __device__ __forceinline__ void words_to_feature_rows(const uint32_t (&w)[16], uint4 (&rows)[4 / E][E])
 {
@@ -191,6 +193,12 @@ __device__ __forceinline__ void feature_rows_to_words(const uint4 (&rows)[4 / E]
     }
 }
 
+__device__ __forceinline__ int vsm_word(int r, int c, int W)
+{
+    const int groups = W >> 2;
+    return r * W + ((((c >> 2) ^ (r >> 4)) & (groups - 1)) << 2) + (c & 3);
+}
+
 template <int E, bool TO_TILED>
 __global__ void __launch_bounds__(kPermThreads)
 permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, PermuteGeom g)
@@ -202,25 +210,30 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
     const int64_t tile_global = blockIdx.x;
     tile_row_offsets(g, tile_global, row_off);
 
-    const int W = g.row_bytes / 4;                            // words per token row
-    const int S = W + 4;                                      // padded row stride (words)
+    const int W = g.row_bytes / 4;                            // words per token row (a power of two, >= 4)
     const int vpr = g.row_bytes / 16;                         // 16-byte vectors per token row
     const int64_t tile_base = tile_global * kTileElems * static_cast<int64_t>(g.row_bytes);
     const int frow = kTileElems * E;                          // bytes of one feature row
+    // work item i of the transposed side: (column group, token group, column in group)
+    auto item = [&](int i, int& c, int& grp) {
+        grp = (i >> 2) & 7;
+        c = ((i >> 5) << 2) + (i & 3);
+    };
 
     if (TO_TILED) {
         for (int i = threadIdx.x; i < kTileElems * vpr; i += kPermThreads) {
             const int r = i / vpr, v = i - r * vpr;
             const int64_t o = row_off[r];
             const uint4 val = o >= 0 ? *reinterpret_cast<const uint4*>(src + o + v * 16) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vsm + r * S + v * 4) = val;
+            *reinterpret_cast<uint4*>(vsm + vsm_word(r, 4 * v, W)) = val;
         }
         __syncthreads();
         for (int i = threadIdx.x; i < W * 8; i += kPermThreads) {
-            const int c = i % W, grp = i / W;
+            int c, grp;
+            item(i, c, grp);
             uint32_t w[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) w[k] = vsm[(grp * 16 + k) * S + c];
+            for (int k = 0; k < 16; ++k) w[k] = vsm[vsm_word(grp * 16 + k, c, W)];
             uint4 rows[F][E];
             words_to_feature_rows<E>(w, rows);
 #pragma unroll
@@ -232,7 +245,8 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
         }
     } else {
         for (int i = threadIdx.x; i < W * 8; i += kPermThreads) {
-            const int c = i % W, grp = i / W;
+            int c, grp;
+            item(i, c, grp);
             uint4 rows[F][E];
 #pragma unroll
             for (int f = 0; f < F; ++f) {
@@ -244,13 +258,13 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
             uint32_t w[16];
             feature_rows_to_words<E>(rows, w);
 #pragma unroll
-            for (int k = 0; k < 16; ++k) vsm[(grp * 16 + k) * S + c] = w[k];
+            for (int k = 0; k < 16; ++k) vsm[vsm_word(grp * 16 + k, c, W)] = w[k];
         }
         __syncthreads();
         for (int i = threadIdx.x; i < kTileElems * vpr; i += kPermThreads) {
             const int r = i / vpr, v = i - r * vpr;
             const int64_t o = row_off[r];
-            if (o >= 0) *reinterpret_cast<uint4*>(dst + o + v * 16) = *reinterpret_cast<const uint4*>(vsm + r * S + v * 4);
+            if (o >= 0) *reinterpret_cast<uint4*>(dst + o + v * 16) = *reinterpret_cast<const uint4*>(vsm + vsm_word(r, 4 * v, W));
         }
     }
 }
@@ -284,9 +298,10 @@ cudaError_t launch_permute_v(const void* src, void* dst, const PermuteGeom& g, i
 {
     const int64_t nblocks = g.B * static_cast<int64_t>(g.heads) * g.ntiles_total;
     if (nblocks <= 0) return cudaSuccess;
-    if (g.row_bytes % 16 != 0 || g.row_bytes > kMaxValueRowBytes || (elem_size != 1 && elem_size != 2))
+    if (g.row_bytes < 16 || g.row_bytes > kMaxValueRowBytes || (g.row_bytes & (g.row_bytes - 1)) != 0 ||
+        (elem_size != 1 && elem_size != 2))
         return cudaErrorNotSupported;
-    const size_t smem = static_cast<size_t>(kTileElems) * (g.row_bytes / 4 + 4) * sizeof(uint32_t);
+    const size_t smem = static_cast<size_t>(kTileElems) * (g.row_bytes / 4) * sizeof(uint32_t);
     dim3 grid(static_cast<unsigned>(nblocks));
     const auto* s = static_cast<const uint8_t*>(src);
     auto* d = static_cast<uint8_t*>(dst);

@@ -131,8 +131,8 @@ gna_status gna_unpermute_tiled(const void* src, void* dst, int B, int heads, con
 /* Raster -> value layout (zero padding) and back (padding dropped): the
  * tiled layout with each tile transposed to d x 128.  Same element count as
  * the tiled layout (gna_tiled_elems).  dtype GNA_BF16 or GNA_FP8_E4M3 with
- * head_dim * element size a multiple of 16 bytes and at most 256 bytes
- * (otherwise GNA_ERR_UNSUPPORTED); src and dst must not overlap.  GNA page
+ * head_dim * element size a power of two from 16 to 256 bytes (otherwise
+ * GNA_ERR_UNSUPPORTED); src and dst must not overlap.  GNA page
  * §2.2 (the permutation is a dedicated copy kernel; here it also produces the
  * operand order of the P V product). */
 gna_status gna_permute_v(const void* src, void* dst, int B, int heads, const int dims[3],

@@ -91,11 +91,12 @@ def test_permute_rejects_bad_arguments_on_host(L):
     assert L.gna_permute(FAKE, FAKE + 4, 1, 1, I3(1, 4, 4), 8, G.GNA_BF16, None) == G.GNA_ERR_INVALID_ARG
     assert L.gna_permute(FAKE, FAKE, 1, 1, I3(1, 4, 4), 8, 7, None) == G.GNA_ERR_INVALID_ARG
     assert L.gna_permute(FAKE, FAKE, 1, 1, I3(1, 4, 4), 3, G.GNA_BF16, None) == G.GNA_ERR_UNSUPPORTED
-    # value layout: 1- or 2-byte elements, rows a multiple of 16 bytes and at most 256
+    # value layout: 1- or 2-byte elements, rows a power of two from 16 to 256 bytes
     assert L.gna_permute_v(None, FAKE, 1, 1, I3(1, 4, 4), 8, G.GNA_BF16, None) == G.GNA_ERR_INVALID_ARG
     assert L.gna_permute_v(FAKE, FAKE, 1, 1, I3(1, 4, 4), 4, G.GNA_F32, None) == G.GNA_ERR_UNSUPPORTED
     assert L.gna_permute_v(FAKE, FAKE, 1, 1, I3(1, 4, 4), 4, G.GNA_BF16, None) == G.GNA_ERR_UNSUPPORTED
     assert L.gna_unpermute_v(FAKE, FAKE, 1, 1, I3(1, 4, 4), 256, G.GNA_BF16, None) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_permute_v(FAKE, FAKE, 1, 1, I3(1, 4, 4), 24, G.GNA_BF16, None) == G.GNA_ERR_UNSUPPORTED
     assert L.gna_permute_tiled(FAKE, FAKE, 1, 1, I3(1, 4, 4), I3(1, 4, 16), 8, G.GNA_BF16,
                                None) == G.GNA_ERR_INVALID_ARG
 

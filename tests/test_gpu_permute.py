@@ -87,8 +87,9 @@ def _bits_gpu(t):
 ])
 def test_value_permute_matches_layout_definition(dtype, B, heads, dims, d, tile):
     esz = torch.tensor([], dtype=dtype).element_size()
-    if (d * esz) % 16 or d * esz > 256:
-        pytest.skip("value layout rows are a multiple of 16 bytes, at most 256")
+    rb = d * esz
+    if rb < 16 or rb > 256 or rb & (rb - 1):
+        pytest.skip("value layout rows are a power of two from 16 to 256 bytes")
     x = torch.from_numpy(normal_raster(8, B, dims, heads, d)).to(dtype)
     t = tile or G.gna_tile_shape(dims)
     want = layout.permute_v_reference(_bits(x), t)
