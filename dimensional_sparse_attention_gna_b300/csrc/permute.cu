@@ -220,12 +220,28 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
         c = ((i >> 5) << 2) + (i & 3);
     };
 
+    // at most 128 rows x 16 vectors = 8 vectors per thread; all loads of a
+    // thread are issued before the first shared-memory store
+    constexpr int kVecPerThread = kTileElems * (kMaxValueRowBytes / 16) / kPermThreads;
     if (TO_TILED) {
-        for (int i = threadIdx.x; i < kTileElems * vpr; i += kPermThreads) {
-            const int r = i / vpr, v = i - r * vpr;
-            const int64_t o = row_off[r];
-            const uint4 val = o >= 0 ? *reinterpret_cast<const uint4*>(src + o + v * 16) : make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(vsm + vsm_word(r, 4 * v, W)) = val;
+        uint4 val[kVecPerThread];
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int i = threadIdx.x + u * kPermThreads;
+            val[u] = make_uint4(0, 0, 0, 0);
+            if (i < kTileElems * vpr) {
+                const int r = i / vpr, v = i - r * vpr;
+                const int64_t o = row_off[r];
+                if (o >= 0) val[u] = __ldcs(reinterpret_cast<const uint4*>(src + o + v * 16));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int i = threadIdx.x + u * kPermThreads;
+            if (i < kTileElems * vpr) {
+                const int r = i / vpr, v = i - r * vpr;
+                *reinterpret_cast<uint4*>(vsm + vsm_word(r, 4 * v, W)) = val[u];
+            }
         }
         __syncthreads();
         for (int i = threadIdx.x; i < W * 8; i += kPermThreads) {
@@ -240,7 +256,7 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
             for (int f = 0; f < F; ++f) {
                 uint4* o = reinterpret_cast<uint4*>(dst + tile_base + static_cast<int64_t>(c * F + f) * frow + grp * 16 * E);
 #pragma unroll
-                for (int e = 0; e < E; ++e) o[e] = rows[f][e];
+                for (int e = 0; e < E; ++e) __stcs(o + e, rows[f][e]);
             }
         }
     } else {
@@ -261,10 +277,23 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
             for (int k = 0; k < 16; ++k) vsm[vsm_word(grp * 16 + k, c, W)] = w[k];
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < kTileElems * vpr; i += kPermThreads) {
-            const int r = i / vpr, v = i - r * vpr;
-            const int64_t o = row_off[r];
-            if (o >= 0) *reinterpret_cast<uint4*>(dst + o + v * 16) = *reinterpret_cast<const uint4*>(vsm + vsm_word(r, 4 * v, W));
+        uint4 val[kVecPerThread];
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int i = threadIdx.x + u * kPermThreads;
+            if (i < kTileElems * vpr) {
+                const int r = i / vpr, v = i - r * vpr;
+                val[u] = *reinterpret_cast<const uint4*>(vsm + vsm_word(r, 4 * v, W));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) {
+            const int i = threadIdx.x + u * kPermThreads;
+            if (i < kTileElems * vpr) {
+                const int r = i / vpr, v = i - r * vpr;
+                const int64_t o = row_off[r];
+                if (o >= 0) *reinterpret_cast<uint4*>(dst + o + v * 16) = val[u];
+            }
         }
     }
 }
