@@ -1,0 +1,96 @@
+"""Edge cases of the CUDA GNA forward against the CPU oracle, every query compared.
+
+Degenerate windows and grids, grids where every tile is padded, a head count far
+above the workloads', e4m3 on a ragged grid, and scores large enough that the
+running maximum jumps by many powers of two between KV tiles (the lazy rescale
+and its overflow guard).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic_inputs import exact_f32, normal_raster, quantize_e4m3, to_bf16
+from tests.gpu_helpers import TOL_BF16_LSE, TOL_BF16_OUT, TOL_FP8, bf16_inputs, compare, gpu_gna, oracle_threads
+
+pytestmark = pytest.mark.gpu
+
+
+def _parity(q, k, v, dims, window, stride, scales=(1.0, 1.0, 1.0), tol_out=TOL_BF16_OUT, tol_lse=TOL_BF16_LSE,
+            descale=None):
+    out, lse = gpu_gna(q, k, v, dims, window, stride, descale=descale)
+    o_ref, l_ref = oracle.forward_c(exact_f32(q), exact_f32(k), exact_f32(v), dims, window, stride,
+                                    tensor_scales=scales, threads=oracle_threads())
+    rel, info = compare(out, lse, o_ref, l_ref, tol_out, tol_lse)
+    return out, lse, rel, info
+
+
+def test_unit_window_returns_own_value_exactly():
+    """w = 1 in every dimension: each query sees only its own key, so out = v
+    (exact: one weight of 1, one bf16 rounding of an exact bf16 value) and
+    lse = scale * <q, k> of that key."""
+    dims, d = (3, 9, 11), 64
+    q, k, v = bf16_inputs(5000, 2, dims, 3, d)
+    out, lse, _, info = _parity(q, k, v, dims, (1, 1, 1), (1, 1, 1))
+    np.testing.assert_array_equal(out, v.float().numpy())
+    qk = (q.double() * k.double()).sum(-1).numpy() / math.sqrt(d)
+    np.testing.assert_allclose(lse, qk, rtol=0, atol=2e-4)
+
+
+def test_single_token_grid():
+    dims = (1, 1, 1)
+    q, k, v = bf16_inputs(5001, 3, dims, 2, 128)
+    out, lse, _, _ = _parity(q, k, v, dims, (1, 1, 1), (1, 1, 1))
+    np.testing.assert_array_equal(out, v.float().numpy())
+
+
+@pytest.mark.parametrize("dims,window,stride", [
+    ((1, 1, 300), (1, 1, 37), (1, 1, 5)),        # a 1-D sequence as a degenerate grid
+    ((1, 300, 1), (1, 64, 1), (1, 8, 1)),
+    ((5, 19, 23), (2, 4, 6), (2, 4, 6)),          # blocked, grid not divisible by the window
+    ((4, 16, 20), (4, 5, 20), (1, 2, 1)),         # window = grid in two dimensions only
+    ((7, 3, 2), (7, 3, 2), (7, 3, 2)),            # one block covering a tiny grid
+])
+def test_degenerate_geometries(dims, window, stride):
+    q, k, v = bf16_inputs(5100 + sum(dims), 1, dims, 2, 64)
+    _, _, rel, info = _parity(q, k, v, dims, window, stride)
+    assert rel < 1.5e-2, info
+
+
+def test_every_tile_padded_many_batches():
+    dims = (3, 5, 7)                               # default tile pads every dimension
+    q, k, v = bf16_inputs(5200, 3, dims, 1, 128)
+    _, _, rel, info = _parity(q, k, v, dims, (3, 3, 5), (1, 2, 2))
+    assert rel < 1.5e-2, info
+
+
+def test_many_heads():
+    dims = (1, 8, 24)
+    q, k, v = bf16_inputs(5300, 1, dims, 64, 64)
+    _, _, rel, info = _parity(q, k, v, dims, (1, 5, 9), (1, 1, 3))
+    assert rel < 1.5e-2, info
+
+
+def test_e4m3_ragged_grid_all_queries():
+    dims, d, heads = (6, 20, 24), 128, 2
+    qs = [quantize_e4m3(normal_raster(5400 + i, 1, dims, heads, d)) for i in range(3)]
+    (q, sq), (k, sk), (v, sv) = qs
+    _, _, rel, info = _parity(q, k, v, dims, (4, 9, 8), (2, 3, 8), scales=(sq, sk, sv), tol_out=TOL_FP8,
+                              tol_lse=TOL_FP8, descale=(sq, sk, sv))
+    assert rel < 0.1, info
+
+
+@pytest.mark.parametrize("amp", [6.0, 24.0])
+def test_large_scores_lazy_rescale(amp):
+    """Q scaled up so that the scores' spread is dozens of natural units: the
+    row maximum keeps jumping between KV tiles, forcing O rescales; with amp 24
+    a jump can exceed 2^64 and the reference must never overflow."""
+    dims, d = (4, 16, 32), 128
+    q32 = normal_raster(5500, 1, dims, 2, d) * amp
+    q = to_bf16(q32)
+    k = to_bf16(normal_raster(5501, 1, dims, 2, d))
+    v = to_bf16(normal_raster(5502, 1, dims, 2, d))
+    out, lse, rel, info = _parity(q, k, v, dims, (3, 9, 17), (1, 1, 1), tol_lse=1e-2 * amp)
+    assert rel < 1.5e-2, info
