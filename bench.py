@@ -163,8 +163,12 @@ class ClockSampler:
             os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
+            # start timing only once the sampler is producing lines
+            t0 = time.time()
+            while time.time() - t0 < 2.0 and os.path.getsize(self.path) == 0:
+                time.sleep(0.02)
         except (OSError, FileNotFoundError):
             self.proc = None
         return self
@@ -394,43 +398,70 @@ def gpu_arm(a, rank, world, local):
         dense_ms = e0.elapsed_time(e1) / reps
         speedup = dense_ms / fwd_ms
 
-    # end to end through the public API with host buffers
+    # end to end through the public API with host buffers: every step copies its
+    # Q, K, V from pinned host memory, runs permute -> forward -> unpermute and
+    # copies O and lse back.  Copies run on their own streams so that step k+1's
+    # upload and step k-1's download overlap step k's kernels (two buffer sets).
     e2e = None
     if not a.no_e2e:
         host_in = [x.cpu().pin_memory() for x in xs]
-        host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        dev_in = [torch.empty_like(x) for x in xs]
+        host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+        host_lse = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
+        dev_in = [[torch.empty_like(x) for x in xs] for _ in range(2)]
+        dev_out = [out, torch.empty_like(out)]
+        dev_lse = [lse, torch.empty_like(lse)]
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev = {name: [torch.cuda.Event() for _ in range(2)] for name in ("in_ready", "perm_done", "comp_done", "out_done")}
+        used = {name: [False, False] for name in ev}
 
-        def e2e_step():
-            for h, dv in zip(host_in, dev_in):
-                dv.copy_(h, non_blocking=True)
-            G.gna_permute(dev_in[0], qt, B, heads, dims, d, stream=stream)
-            G.gna_permute(dev_in[1], kt, B, heads, dims, d, stream=stream)
-            G.gna_permute_v(dev_in[2], vt, B, heads, dims, d, stream=stream)
+        def e2e_step(k):
+            b = k % 2
+            if used["perm_done"][b]:
+                s_in.wait_event(ev["perm_done"][b])       # inputs of step k-2 consumed
+            with torch.cuda.stream(s_in):
+                for h, dv in zip(host_in, dev_in[b]):
+                    dv.copy_(h, non_blocking=True)
+            ev["in_ready"][b].record(s_in)
+            stream.wait_event(ev["in_ready"][b])
+            G.gna_permute(dev_in[b][0], qt, B, heads, dims, d, stream=stream)
+            G.gna_permute(dev_in[b][1], kt, B, heads, dims, d, stream=stream)
+            G.gna_permute_v(dev_in[b][2], vt, B, heads, dims, d, stream=stream)
+            ev["perm_done"][b].record(stream)
+            used["perm_done"][b] = True
             G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds,
                           stream=stream)
-            G.gna_unpermute(out_t, out, B, heads, dims, d, stream=stream)
-            G.gna_unpermute(lse_t.unsqueeze(-1), lse, B, heads, dims, 1, stream=stream)
-            host_out.copy_(out, non_blocking=True)
-            host_lse.copy_(lse, non_blocking=True)
-        e2e_step()
+            if used["out_done"][b]:
+                stream.wait_event(ev["out_done"][b])      # results of step k-2 downloaded
+            G.gna_unpermute(out_t, dev_out[b], B, heads, dims, d, stream=stream)
+            G.gna_unpermute(lse_t.unsqueeze(-1), dev_lse[b], B, heads, dims, 1, stream=stream)
+            ev["comp_done"][b].record(stream)
+            s_out.wait_event(ev["comp_done"][b])
+            with torch.cuda.stream(s_out):
+                host_out[b].copy_(dev_out[b], non_blocking=True)
+                host_lse[b].copy_(dev_lse[b], non_blocking=True)
+            ev["out_done"][b].record(s_out)
+            used["out_done"][b] = True
+        for k in range(2):
+            e2e_step(k)
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2e_steps = max(3, min(a.steps, 5))
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+        e2e_steps = max(4, min(a.steps, 8))
+        e0.record(s_in)
+        for k in range(e2e_steps):
+            e2e_step(k)
+        e1.record(s_out)
         torch.cuda.synchronize()
         barrier(world)
+        G.gna_get_status(stream)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
         e2e_val = sum_over_ranks(flops_rank * e2e_steps, world) / (e2e_ms / 1e3) / 1e12
         e2e = {"value": e2e_val, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(sum(x.numel() * x.element_size() for x in host_in)),
-               "d2h_bytes_per_step": int(host_out.numel() * host_out.element_size()
-                                         + host_lse.numel() * host_lse.element_size())}
+               "d2h_bytes_per_step": int(host_out[0].numel() * host_out[0].element_size()
+                                         + host_lse[0].numel() * host_lse[0].element_size()),
+               "ms_per_step": e2e_ms / e2e_steps,
+               "pipelining": "uploads, kernels and downloads of consecutive steps on three streams"}
 
     clk = clocks.summary()
     traffic = kernel_traffic(1, heads, B)
