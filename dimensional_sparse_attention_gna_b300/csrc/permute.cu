@@ -120,14 +120,14 @@ permute_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Permu
 }
 
 // Raster <-> value layout for elements of E bytes (E = 1 or 2; rows of a
-// power of two from 16 to 256 bytes).  Shared memory holds the tile token-major,
-// [128 tokens][W words] (W = d*E/4), with the 16-byte groups of token r stored
-// at group index (group ^ (r / 16) mod (W / 4)).  On the transposed side a
-// thread owns word column c (features 4/E*c ..) of a group of 16 tokens: 16*E
-// contiguous bytes of each of its 4/E feature rows.  Eight consecutive lanes
-// take the eight token groups of one column, so a warp writes (or reads) whole
-// 128*E-byte feature rows, and the XOR spreads those eight lanes over distinct
-// banks.
+// power of two from 16 to 256 bytes).  A block moves one half tile (64 tokens):
+// shared memory holds it token-major, [64 tokens][W words] (W = d*E/4), with
+// the 16-byte groups XOR-swizzled by token group (vsm_word).  On the
+// transposed side a thread owns word column c (features 4/E*c ..) of a group
+// of 16 tokens: 16*E contiguous bytes of each of its 4/E feature rows.  Four
+// consecutive lanes take the four token groups of one column, so a warp writes
+// (or reads) 64*E contiguous bytes of each feature row it touches, and the
+// swizzle keeps its shared-memory accesses on distinct banks.
 template <int E>
 __device__ __forceinline__ void words_to_feature_rows(const uint32_t (&w)[16], uint4 (&rows)[4 / E][E])
 {
@@ -193,58 +193,67 @@ __device__ __forceinline__ void feature_rows_to_words(const uint4 (&rows)[4 / E]
     }
 }
 
+// Word (token r of the half tile, column c) in shared memory: rows of W words;
+// 16-byte group g of token r sits at group g ^ 2 * (r / 16) (mod W / 4).
 __device__ __forceinline__ int vsm_word(int r, int c, int W)
 {
     const int groups = W >> 2;
-    return r * W + ((((c >> 2) ^ (r >> 4)) & (groups - 1)) << 2) + (c & 3);
+    return r * W + ((((c >> 2) ^ ((r >> 4) << 1)) & (groups - 1)) << 2) + (c & 3);
 }
 
+constexpr int kVThreads = 128;          // one block moves half a tile: 64 tokens
+constexpr int kVTokens = kTileElems / 2;
+
 template <int E, bool TO_TILED>
-__global__ void __launch_bounds__(kPermThreads)
+__global__ void __launch_bounds__(kVThreads)
 permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, PermuteGeom g)
 {
     constexpr int F = 4 / E;                                  // features per 32-bit word
     extern __shared__ __align__(16) uint32_t vsm[];
     __shared__ int64_t row_off[kTileElems];
 
-    const int64_t tile_global = blockIdx.x;
+    const int64_t tile_global = blockIdx.x >> 1;
+    const int hh = blockIdx.x & 1;                            // which 64 tokens of the tile
     tile_row_offsets(g, tile_global, row_off);
 
     const int W = g.row_bytes / 4;                            // words per token row (a power of two, >= 4)
     const int vpr = g.row_bytes / 16;                         // 16-byte vectors per token row
     const int64_t tile_base = tile_global * kTileElems * static_cast<int64_t>(g.row_bytes);
     const int frow = kTileElems * E;                          // bytes of one feature row
-    // work item i of the transposed side: (column group, token group, column in group)
+    // work item i of the transposed side: (column group, token group, column in group);
+    // four token groups of 16 per half tile
     auto item = [&](int i, int& c, int& grp) {
-        grp = (i >> 2) & 7;
-        c = ((i >> 5) << 2) + (i & 3);
+        grp = (i >> 2) & 3;
+        c = ((i >> 4) << 2) + (i & 3);
     };
+    const int nvec = kVTokens * vpr;
+    const int nitem = W * 4;
 
-    // at most 128 rows x 16 vectors = 8 vectors per thread; all loads of a
+    // at most 64 rows x 16 vectors = 8 vectors per thread; all loads of a
     // thread are issued before the first shared-memory store
-    constexpr int kVecPerThread = kTileElems * (kMaxValueRowBytes / 16) / kPermThreads;
+    constexpr int kVecPerThread = kVTokens * (kMaxValueRowBytes / 16) / kVThreads;
     if (TO_TILED) {
         uint4 val[kVecPerThread];
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
-            const int i = threadIdx.x + u * kPermThreads;
+            const int i = threadIdx.x + u * kVThreads;
             val[u] = make_uint4(0, 0, 0, 0);
-            if (i < kTileElems * vpr) {
+            if (i < nvec) {
                 const int r = i / vpr, v = i - r * vpr;
-                const int64_t o = row_off[r];
+                const int64_t o = row_off[hh * kVTokens + r];
                 if (o >= 0) val[u] = __ldcs(reinterpret_cast<const uint4*>(src + o + v * 16));
             }
         }
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
-            const int i = threadIdx.x + u * kPermThreads;
-            if (i < kTileElems * vpr) {
+            const int i = threadIdx.x + u * kVThreads;
+            if (i < nvec) {
                 const int r = i / vpr, v = i - r * vpr;
                 *reinterpret_cast<uint4*>(vsm + vsm_word(r, 4 * v, W)) = val[u];
             }
         }
         __syncthreads();
-        for (int i = threadIdx.x; i < W * 8; i += kPermThreads) {
+        for (int i = threadIdx.x; i < nitem; i += kVThreads) {
             int c, grp;
             item(i, c, grp);
             uint32_t w[16];
@@ -252,22 +261,24 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
             for (int k = 0; k < 16; ++k) w[k] = vsm[vsm_word(grp * 16 + k, c, W)];
             uint4 rows[F][E];
             words_to_feature_rows<E>(w, rows);
+            const int tok0 = hh * kVTokens + grp * 16;
 #pragma unroll
             for (int f = 0; f < F; ++f) {
-                uint4* o = reinterpret_cast<uint4*>(dst + tile_base + static_cast<int64_t>(c * F + f) * frow + grp * 16 * E);
+                uint4* o = reinterpret_cast<uint4*>(dst + tile_base + static_cast<int64_t>(c * F + f) * frow + tok0 * E);
 #pragma unroll
                 for (int e = 0; e < E; ++e) __stcs(o + e, rows[f][e]);
             }
         }
     } else {
-        for (int i = threadIdx.x; i < W * 8; i += kPermThreads) {
+        for (int i = threadIdx.x; i < nitem; i += kVThreads) {
             int c, grp;
             item(i, c, grp);
             uint4 rows[F][E];
+            const int tok0 = hh * kVTokens + grp * 16;
 #pragma unroll
             for (int f = 0; f < F; ++f) {
                 const uint4* o =
-                    reinterpret_cast<const uint4*>(src + tile_base + static_cast<int64_t>(c * F + f) * frow + grp * 16 * E);
+                    reinterpret_cast<const uint4*>(src + tile_base + static_cast<int64_t>(c * F + f) * frow + tok0 * E);
 #pragma unroll
                 for (int e = 0; e < E; ++e) rows[f][e] = o[e];
             }
@@ -280,18 +291,18 @@ permute_v_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, Per
         uint4 val[kVecPerThread];
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
-            const int i = threadIdx.x + u * kPermThreads;
-            if (i < kTileElems * vpr) {
+            const int i = threadIdx.x + u * kVThreads;
+            if (i < nvec) {
                 const int r = i / vpr, v = i - r * vpr;
                 val[u] = *reinterpret_cast<const uint4*>(vsm + vsm_word(r, 4 * v, W));
             }
         }
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
-            const int i = threadIdx.x + u * kPermThreads;
-            if (i < kTileElems * vpr) {
+            const int i = threadIdx.x + u * kVThreads;
+            if (i < nvec) {
                 const int r = i / vpr, v = i - r * vpr;
-                const int64_t o = row_off[r];
+                const int64_t o = row_off[hh * kVTokens + r];
                 if (o >= 0) *reinterpret_cast<uint4*>(dst + o + v * 16) = val[u];
             }
         }
@@ -330,16 +341,17 @@ cudaError_t launch_permute_v(const void* src, void* dst, const PermuteGeom& g, i
     if (g.row_bytes < 16 || g.row_bytes > kMaxValueRowBytes || (g.row_bytes & (g.row_bytes - 1)) != 0 ||
         (elem_size != 1 && elem_size != 2))
         return cudaErrorNotSupported;
-    const size_t smem = static_cast<size_t>(kTileElems) * (g.row_bytes / 4) * sizeof(uint32_t);
-    dim3 grid(static_cast<unsigned>(nblocks));
+    const size_t smem = static_cast<size_t>(kVTokens) * (g.row_bytes / 4) * sizeof(uint32_t);
+    if (2 * nblocks > INT32_MAX) return cudaErrorNotSupported;
+    dim3 grid(static_cast<unsigned>(2 * nblocks));
     const auto* s = static_cast<const uint8_t*>(src);
     auto* d = static_cast<uint8_t*>(dst);
     if (elem_size == 2) {
-        if (to_tiled) permute_v_kernel<2, true><<<grid, kPermThreads, smem, stream>>>(s, d, g);
-        else permute_v_kernel<2, false><<<grid, kPermThreads, smem, stream>>>(s, d, g);
+        if (to_tiled) permute_v_kernel<2, true><<<grid, kVThreads, smem, stream>>>(s, d, g);
+        else permute_v_kernel<2, false><<<grid, kVThreads, smem, stream>>>(s, d, g);
     } else {
-        if (to_tiled) permute_v_kernel<1, true><<<grid, kPermThreads, smem, stream>>>(s, d, g);
-        else permute_v_kernel<1, false><<<grid, kPermThreads, smem, stream>>>(s, d, g);
+        if (to_tiled) permute_v_kernel<1, true><<<grid, kVThreads, smem, stream>>>(s, d, g);
+        else permute_v_kernel<1, false><<<grid, kVThreads, smem, stream>>>(s, d, g);
     }
     return cudaGetLastError();
 }
