@@ -279,6 +279,20 @@ __device__ __forceinline__ void tmem_store_n(uint32_t taddr, const uint32_t* r)
     }
 }
 
+// Load N (16, 32 or 64) consecutive 32-bit TMEM columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_ld_n(uint32_t taddr, uint32_t (&r)[N])
+{
+    if constexpr (N == 64) {
+        tmem_ld64(taddr, r);
+    } else if constexpr (N == 32) {
+        tmem_ld32(taddr, r);
+    } else {
+        static_assert(N == 16, "16, 32 or 64 columns");
+        tmem_ld16(taddr, r);
+    }
+}
+
 // Multiply O columns [0, N) at taddr of this thread's row by alpha (N multiple of 16).
 template <int N>
 __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha)
@@ -556,9 +570,8 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             float mx = -INFINITY;
             if (ok) {
                 tc_fence_after();
-                uint32_t r0[32], r1[32];
-                tmem_ld32(t_s + half * 64, r0);
-                tmem_ld32(t_s + half * 64 + 32, r1);
+                uint32_t rs[64];
+                tmem_ld64(t_s + half * 64, rs);
                 // while the scores travel from TMEM: is this KV tile partial?
                 bool full = true;
 #pragma unroll
@@ -585,13 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                                      ? 0.0f : -INFINITY;
                     }
                     tmem_wait_ld();
-                    reg_fence(r0);
-                    reg_fence(r1);
+                    reg_fence(rs);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        s[i] = __uint_as_float(r0[i]);
-                        s[32 + i] = __uint_as_float(r1[i]);
-                    }
+                    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(rs[i]);
                     if (!full) {
 #pragma unroll
                         for (int c = 0; c < 64; c += 2) {
@@ -608,13 +617,9 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                         m1 = row_mask_word(p, 2 * half + 1, lo_t, lo_y, lo_x);
                     }
                     tmem_wait_ld();
-                    reg_fence(r0);
-                    reg_fence(r1);
+                    reg_fence(rs);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        s[i] = __uint_as_float(r0[i]);
-                        s[32 + i] = __uint_as_float(r1[i]);
-                    }
+                    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(rs[i]);
                     if (!full) {
 #pragma unroll
                         for (int c = 0; c < 32; ++c) {
@@ -706,17 +711,18 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             const bool has = row_valid && l_tot > 0.0f;
             const float inv_l = has ? out_scale / l_tot : 0.0f;
             uint8_t* out_row = static_cast<uint8_t*>(p.out) + (q_tile_global * kTileElems + row) * (D * 2) + half * D;
+            // this half of the O row in one TMEM load (16, 32 or 64 columns)
+            uint32_t r[C::kOHalf];
+            tmem_ld_n<C::kOHalf>(t_ohalf, r);
+            tmem_wait_ld();
+            reg_fence(r);
 #pragma unroll
             for (int c = 0; c < C::kOHalf; c += 16) {
-                uint32_t r[16];
-                tmem_ld16(t_ohalf + c, r);
-                tmem_wait_ld();
-                reg_fence(r);
                 uint32_t pk[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * inv_l,
-                                                             __uint_as_float(r[2 * i + 1]) * inv_l);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[c + 2 * i]) * inv_l,
+                                                             __uint_as_float(r[c + 2 * i + 1]) * inv_l);
                     pk[i] = *reinterpret_cast<uint32_t*>(&h);
                 }
                 uint4* dst = reinterpret_cast<uint4*>(out_row + c * 2);
