@@ -500,6 +500,7 @@ def gpu_arm(a, rank, world, local):
         "unpermute_gbps": unperm_bytes / (unperm_ms / 1e3) / 1e9,
         "dense_forward_ms": dense_ms, "speedup_vs_dense": speedup,
         "flop_sparsity_ratio": n_ratio,
+        "speedup_bound_at_equal_tile_rate": G.gna_plan_tile(dims, a.window, a.stride)[2],
         "speedup_over_ratio": None if speedup is None else speedup / n_ratio,
         "e2e": e2e, "gpu_launches": launches_per_step * a.steps, "clocks": clk, "cpu_baseline": cpu,
     }

@@ -349,6 +349,50 @@ gna_status gna_tile_stats(const int dims[3], const int window[3], const int stri
     return GNA_OK;
 }
 
+gna_status gna_plan_tile(const int dims[3], const int window[3], const int stride[3], int leader_rule, int tile[3],
+                         double* tile_overhead, double* speedup_bound)
+{
+    gna_status st = check_geometry(dims, window, stride);
+    if (st != GNA_OK) return st;
+    if (tile == nullptr) return fail(GNA_ERR_INVALID_ARG, "tile is NULL");
+    if (leader_rule != GNA_LEADER_CENTER && leader_rule != GNA_LEADER_LITERAL)
+        return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", leader_rule);
+    // every 128-element power-of-two tile; fewest visited 128 x 128 tiles
+    // wins, then fewest partial tiles, then the default tile of the grid
+    int def[3];
+    default_tile(dims, def);
+    int64_t best_v = -1, best_p = 0;
+    int best[3] = {def[0], def[1], def[2]};
+    for (int lt = 0; lt <= 7; ++lt)
+        for (int lh = 0; lt + lh <= 7; ++lh) {
+            const int t[3] = {1 << lt, 1 << lh, 1 << (7 - lt - lh)};
+            int64_t v = 0, pa = 0, nq = 0;
+            if (gna_tile_stats(dims, window, stride, t, leader_rule, &v, &pa, &nq) != GNA_OK) continue;
+            const bool is_def = t[0] == def[0] && t[1] == def[1] && t[2] == def[2];
+            if (best_v < 0 || v < best_v || (v == best_v && (pa < best_p || (pa == best_p && is_def)))) {
+                best_v = v;
+                best_p = pa;
+                best[0] = t[0];
+                best[1] = t[1];
+                best[2] = t[2];
+            }
+        }
+    tile[0] = best[0];
+    tile[1] = best[1];
+    tile[2] = best[2];
+    double useful = 1.0, tiles_q = 1.0;
+    for (int d = 0; d < 3; ++d) {
+        useful *= static_cast<double>(dims[d]) * window[d];
+        tiles_q *= (dims[d] + best[d] - 1) / best[d];
+    }
+    const double tile_pairs = static_cast<double>(gna::kTileElems) * gna::kTileElems;
+    if (tile_overhead) *tile_overhead = static_cast<double>(best_v) * tile_pairs / useful;
+    // dense attention on the same tiling visits every KV tile from every Q tile
+    if (speedup_bound) *speedup_bound = tiles_q * tiles_q / static_cast<double>(best_v);
+    t_last_error.clear();
+    return GNA_OK;
+}
+
 gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
                           const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
                           const gna_options* opt, void* stream)

@@ -94,6 +94,9 @@ def lib() -> ctypes.CDLL:
         L.gna_tile_stats.restype = st
         L.gna_tile_stats.argtypes = [_I3, _I3, _I3, _P, _INT, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
+        L.gna_plan_tile.restype = st
+        L.gna_plan_tile.argtypes = [_I3, _I3, _I3, _INT, _I3, ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double)]
         L.gna_get_status.restype = st
         L.gna_get_status.argtypes = [_P]
         _lib = L
@@ -260,6 +263,16 @@ def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADE
     _check(lib().gna_tile_stats(_I3(*dims), _I3(*window), _I3(*stride), t, leader_rule,
                                 ctypes.byref(v), ctypes.byref(p_), ctypes.byref(q)))
     return v.value, p_.value, q.value
+
+
+def gna_plan_tile(dims, window, stride, leader_rule: int = GNA_LEADER_CENTER):
+    """(tile, tile_overhead, speedup_bound): the tile with the fewest visited 128 x 128
+    tiles, its visited-over-useful work ratio and its speedup bound over dense attention."""
+    t = _I3()
+    ov, sp = ctypes.c_double(), ctypes.c_double()
+    _check(lib().gna_plan_tile(_I3(*dims), _I3(*window), _I3(*stride), leader_rule, t, ctypes.byref(ov),
+                               ctypes.byref(sp)))
+    return tuple(t), ov.value, sp.value
 
 
 def gna_get_status(stream=None):

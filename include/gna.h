@@ -179,6 +179,21 @@ gna_status gna_tile_stats(const int dims[3], const int window[3], const int stri
                           const int tile[3], int leader_rule,
                           int64_t* visited_kv_tiles, int64_t* partial_kv_tiles, int64_t* q_tiles);
 
+/* Tile planner: the analytic speedup bound the GNA page suggests checking before
+ * deployment (§4.2, problem 2; a NATTENSim-like count).  Over every 128-element
+ * power-of-two tile it counts, with gna_tile_stats, the 128 x 128 tiles the
+ * forward pass visits and picks the tile with the fewest (ties: fewer partial
+ * tiles, then the default tile).  Outputs:
+ *   tile          the chosen tile (use it with the *_tiled permutes and
+ *                 gna_forward_ex);
+ *   tile_overhead visited tile pairs / useful (query, key) pairs, >= 1 (NULL ok);
+ *   speedup_bound dense attention's visited tiles / these visited tiles on the
+ *                 same tiling: the speedup over dense attention at equal
+ *                 tile throughput (NULL ok).
+ * Host only.  GNA_ERR_INVALID_ARG on bad geometry or leader rule. */
+gna_status gna_plan_tile(const int dims[3], const int window[3], const int stride[3], int leader_rule,
+                         int tile[3], double* tile_overhead, double* speedup_bound);
+
 /* ------------------------------------------------------------ status ---- */
 
 /* Synchronises `stream`, then returns and clears the device status word

@@ -7,6 +7,7 @@
   element mask) against a brute-force count built from the oracle's window rule.
 """
 import ctypes
+import math
 import itertools
 import os
 import re
@@ -174,3 +175,36 @@ def test_blocked_window_aligned_with_tiles_needs_no_mask(L):
     assert partial == 0 or (visited, partial, nq)[1] >= 0
     visited, partial, nq = G.gna_tile_stats((32, 48, 96), (16, 32, 48), (16, 32, 48), (2, 8, 8))
     assert partial == 0 and visited == nq * (16 // 2) * (32 // 8) * (48 // 8)
+
+
+@pytest.mark.parametrize("dims,window,stride", [
+    ((30, 48, 80), (16, 32, 48), (1, 1, 1)),
+    ((30, 48, 80), (16, 32, 48), (16, 8, 8)),
+    ((1, 256, 256), (1, 64, 64), (1, 1, 1)),
+    ((1, 256, 256), (1, 64, 64), (1, 16, 16)),
+    ((6, 20, 24), (4, 9, 8), (2, 3, 8)),
+])
+def test_plan_tile_is_the_minimum_over_all_tiles(L, dims, window, stride):
+    """The planner's tile visits no more tiles than any other 128-element tile, and its
+    reported ratios follow from the brute-force tile counts."""
+    tile, overhead, speedup = G.gna_plan_tile(dims, window, stride)
+    assert np.prod(tile) == 128
+    visited = {}
+    for lt in range(8):
+        for lh in range(8 - lt):
+            t = (1 << lt, 1 << lh, 1 << (7 - lt - lh))
+            visited[t] = G.gna_tile_stats(dims, window, stride, t)[0]
+    assert visited[tuple(tile)] == min(visited.values())
+    useful = np.prod(dims) * np.prod(window)
+    assert math.isclose(overhead, visited[tuple(tile)] * 128 * 128 / useful, rel_tol=1e-12)
+    nq = np.prod([-(-L_ // t_) for L_, t_ in zip(dims, tile)])
+    assert math.isclose(speedup, nq * nq / visited[tuple(tile)], rel_tol=1e-12)
+    assert overhead >= 1.0 and speedup <= np.prod(dims) / np.prod(window) * overhead + 1e-9
+
+
+def test_plan_tile_blocked_aligned_is_exact(L):
+    """Stride = window with the window a multiple of a tile: no wasted pair, and the
+    bound equals the FLOP ratio N / |W| (GNA page §1.1, perfectly block-sparse)."""
+    tile, overhead, speedup = G.gna_plan_tile((32, 48, 96), (16, 32, 48), (16, 32, 48))
+    assert overhead == 1.0
+    assert math.isclose(speedup, 32 * 48 * 96 / (16 * 32 * 48), rel_tol=1e-12)
