@@ -56,6 +56,8 @@ def parse_args(argv=None):
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
+    ap.add_argument("--sustain", type=float, default=0.0,
+                    help="also run the forward back to back for this many seconds and report the sustained rate")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
@@ -464,6 +466,28 @@ def gpu_arm(a, rank, world, local):
                "pipelining": "uploads, kernels and downloads of consecutive steps on three streams"}
 
     clk = clocks.summary()
+
+    # optional: the forward launched back to back for several seconds, long
+    # enough for the board to reach its average power cap
+    sustained = None
+    if a.sustain > 0:
+        with ClockSampler(gpu_index) as sclk:
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            n_sus, t_wall = 0, time.time()
+            s0.record(stream)
+            while time.time() - t_wall < a.sustain:
+                for _ in range(5):
+                    G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds,
+                                  stream=stream)
+                n_sus += 5
+                stream.synchronize()
+            s1.record(stream)
+            torch.cuda.synchronize()
+        G.gna_get_status(stream)
+        sus_ms = s0.elapsed_time(s1) / n_sus
+        sustained = {"value": flops_rank / (sus_ms / 1e3) / 1e12, "unit": "TFLOP/s", "launches": n_sus,
+                     "forward_ms": sus_ms, "seconds": a.sustain, "clocks": sclk.summary(),
+                     "frac_of_sustained_peak": flops_rank / (sus_ms / 1e3) / 1e12 / peak_sustained}
     traffic = kernel_traffic(1, heads, B)
 
     cpu = None
@@ -503,6 +527,7 @@ def gpu_arm(a, rank, world, local):
         "speedup_bound_at_equal_tile_rate": G.gna_plan_tile(dims, a.window, a.stride)[2],
         "speedup_over_ratio": None if speedup is None else speedup / n_ratio,
         "e2e": e2e, "gpu_launches": launches_per_step * a.steps, "clocks": clk, "cpu_baseline": cpu,
+        "sustained": sustained,
     }
     print(json.dumps(line), flush=True)
 
