@@ -337,7 +337,10 @@ gna_status gna_tile_stats(const int dims[3], const int window[3], const int stri
         for (int qt = 0; qt < nt; ++qt) {
             const gna::DimRange r = gna::dim_range(qt, tile[d], dims[d], window[d], stride[d], off);
             sum_cnt += r.k1 - r.k0 + 1;
-            for (int kt = r.k0; kt <= r.k1; ++kt) sum_full += gna::dim_tile_full(kt, tile[d], dims[d], window[d], r);
+            // the kernel's full-tile test: the interval form of dim_tile_full
+            int flo, fhi;
+            gna::dim_full_range(tile[d], dims[d], window[d], r, flo, fhi);
+            for (int kt = r.k0; kt <= r.k1; ++kt) sum_full += (kt >= flo && kt <= fhi);
         }
         visited *= sum_cnt;
         full *= sum_full;

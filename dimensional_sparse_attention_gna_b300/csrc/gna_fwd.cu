@@ -158,16 +158,11 @@ __device__ __forceinline__ void raise_status(volatile int* abort_flag)
     atomicExch(&g_device_status, 4 /* GNA_ERR_TIMEOUT */);
 }
 
-// KV tile visited at loop index j (row-major over the box).
+// Box of KV tiles a Q tile visits (row-major), and per dimension the interval
+// of KV tiles that lie inside every window of the Q tile.
 struct KvBox {
     int k0[3], cnt[3];
-    DimRange r[3];
-    __device__ __forceinline__ void coords(int j, int (&kc)[3]) const
-    {
-        kc[2] = k0[2] + j % cnt[2];
-        kc[1] = k0[1] + (j / cnt[2]) % cnt[1];
-        kc[0] = k0[0] + j / (cnt[2] * cnt[1]);
-    }
+    int full_lo[3], full_hi[3];
 };
 
 __device__ __forceinline__ void advance_odometer(int (&kc)[3], const KvBox& box)
@@ -337,9 +332,10 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     KvBox box;
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
-        box.r[d] = dim_range(qc[d], p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
-        box.k0[d] = box.r[d].k0;
-        box.cnt[d] = box.r[d].k1 - box.r[d].k0 + 1;
+        const DimRange r = dim_range(qc[d], p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
+        box.k0[d] = r.k0;
+        box.cnt[d] = r.k1 - r.k0 + 1;
+        dim_full_range(p.tile[d], p.dims[d], p.win[d], r, box.full_lo[d], box.full_hi[d]);
     }
     const int n_kv = box.cnt[0] * box.cnt[1] * box.cnt[2];
     const int64_t kv_row_base = bh * p.tiles_per_head * kTileElems;
@@ -575,33 +571,32 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                 // while the scores travel from TMEM: is this KV tile partial?
                 bool full = true;
 #pragma unroll
-                for (int d = 0; d < 3; ++d)
-                    full = full && dim_tile_full(kc[d], p.tile[d], p.dims[d], p.win[d], box.r[d]);
+                for (int d = 0; d < 3; ++d) full = full && kc[d] >= box.full_lo[d] && kc[d] <= box.full_hi[d];
                 const int lo_t = st[0] - kc[0] * p.tile[0];
                 const int lo_y = st[1] - kc[1] * p.tile[1];
                 const int lo_x = st[2] - kc[2] * p.tile[2];
                 if constexpr (TW > 0) {
-                    // element (ct, cy, cx) of the tile is masked iff one of
-                    // its coordinates leaves the row's window: add -inf
-                    // biases per x position and per (t, y) group of TW columns
-                    constexpr int GPH = 64 / TW;          // (t, y) groups per half row
-                    float bx[TW], bg[GPH];
-#pragma unroll
-                    for (int cx = 0; cx < TW; ++cx)
-                        bx[cx] = static_cast<unsigned>(cx - lo_x) < static_cast<unsigned>(p.win[2]) ? 0.0f : -INFINITY;
-#pragma unroll
-                    for (int gi = 0; gi < GPH; ++gi) {
-                        const int g = half * GPH + gi;
-                        const int cy = g % TH, ct = g / TH;
-                        bg[gi] = (static_cast<unsigned>(ct - lo_t) < static_cast<unsigned>(p.win[0]) &&
-                                  static_cast<unsigned>(cy - lo_y) < static_cast<unsigned>(p.win[1]))
-                                     ? 0.0f : -INFINITY;
-                    }
                     tmem_wait_ld();
                     reg_fence(rs);
 #pragma unroll
                     for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(rs[i]);
                     if (!full) {
+                        // element (ct, cy, cx) of the tile is masked iff one of
+                        // its coordinates leaves the row's window: add -inf
+                        // biases per x position and per (t, y) group of TW columns
+                        constexpr int GPH = 64 / TW;      // (t, y) groups per half row
+                        float bx[TW], bg[GPH];
+#pragma unroll
+                        for (int cx = 0; cx < TW; ++cx)
+                            bx[cx] = static_cast<unsigned>(cx - lo_x) < static_cast<unsigned>(p.win[2]) ? 0.0f : -INFINITY;
+#pragma unroll
+                        for (int gi = 0; gi < GPH; ++gi) {
+                            const int g = half * GPH + gi;
+                            const int cy = g % TH, ct = g / TH;
+                            bg[gi] = (static_cast<unsigned>(ct - lo_t) < static_cast<unsigned>(p.win[0]) &&
+                                      static_cast<unsigned>(cy - lo_y) < static_cast<unsigned>(p.win[1]))
+                                         ? 0.0f : -INFINITY;
+                        }
 #pragma unroll
                         for (int c = 0; c < 64; c += 2) {
                             float2 v = fadd2(make_float2(s[c], s[c + 1]), make_float2(bx[c % TW], bx[(c + 1) % TW]));

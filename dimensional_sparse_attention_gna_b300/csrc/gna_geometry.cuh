@@ -67,4 +67,14 @@ __host__ __device__ __forceinline__ bool dim_tile_full(int kt, int t, int L, int
     return lo >= r.smax && hi <= r.smin + w - 1 && hi < L;
 }
 
+// The KV tiles along this dimension for which dim_tile_full holds form one
+// interval [lo, hi] (empty when hi < lo): tile kt is full iff
+// kt * t >= r.smax and kt * t + t <= min(r.smin + w, L).
+__host__ __device__ __forceinline__ void dim_full_range(int t, int L, int w, const DimRange& r, int& lo, int& hi)
+{
+    lo = (r.smax + t - 1) / t;
+    const int end = (r.smin + w < L ? r.smin + w : L) - t;     // last allowed tile start
+    hi = end >= 0 ? end / t : -1;
+}
+
 }  // namespace gna
