@@ -569,9 +569,11 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                 uint32_t rs[64];
                 tmem_ld64(t_s + half * 64, rs);
                 // while the scores travel from TMEM: is this KV tile partial?
-                bool full = true;
+                // per dimension: does this KV tile lie inside every window of the Q tile?
+                bool fd[3];
 #pragma unroll
-                for (int d = 0; d < 3; ++d) full = full && kc[d] >= box.full_lo[d] && kc[d] <= box.full_hi[d];
+                for (int d = 0; d < 3; ++d) fd[d] = kc[d] >= box.full_lo[d] && kc[d] <= box.full_hi[d];
+                const bool full = fd[0] && fd[1] && fd[2];
                 const int lo_t = st[0] - kc[0] * p.tile[0];
                 const int lo_y = st[1] - kc[1] * p.tile[1];
                 const int lo_x = st[2] - kc[2] * p.tile[2];
@@ -580,15 +582,25 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                     reg_fence(rs);
 #pragma unroll
                     for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(rs[i]);
-                    if (!full) {
-                        // element (ct, cy, cx) of the tile is masked iff one of
-                        // its coordinates leaves the row's window: add -inf
-                        // biases per x position and per (t, y) group of TW columns
-                        constexpr int GPH = 64 / TW;      // (t, y) groups per half row
-                        float bx[TW], bg[GPH];
+                    // element (ct, cy, cx) of the tile is masked iff one of its
+                    // coordinates leaves the row's window: -inf biases per x
+                    // position (only if x is partial) and per (t, y) group of
+                    // TW columns (only if t or y is partial)
+                    if (!fd[2]) {
+                        float bx[TW];
 #pragma unroll
                         for (int cx = 0; cx < TW; ++cx)
                             bx[cx] = static_cast<unsigned>(cx - lo_x) < static_cast<unsigned>(p.win[2]) ? 0.0f : -INFINITY;
+#pragma unroll
+                        for (int c = 0; c < 64; c += 2) {
+                            const float2 v = fadd2(make_float2(s[c], s[c + 1]), make_float2(bx[c % TW], bx[(c + 1) % TW]));
+                            s[c] = v.x;
+                            s[c + 1] = v.y;
+                        }
+                    }
+                    if (!(fd[0] && fd[1])) {
+                        constexpr int GPH = 64 / TW;      // (t, y) groups per half row
+                        float bg[GPH];
 #pragma unroll
                         for (int gi = 0; gi < GPH; ++gi) {
                             const int g = half * GPH + gi;
@@ -599,8 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                         }
 #pragma unroll
                         for (int c = 0; c < 64; c += 2) {
-                            float2 v = fadd2(make_float2(s[c], s[c + 1]), make_float2(bx[c % TW], bx[(c + 1) % TW]));
-                            v = fadd2(v, make_float2(bg[c / TW], bg[c / TW]));
+                            const float2 v = fadd2(make_float2(s[c], s[c + 1]), make_float2(bg[c / TW], bg[c / TW]));
                             s[c] = v.x;
                             s[c + 1] = v.y;
                         }
