@@ -94,3 +94,28 @@ def test_large_scores_lazy_rescale(amp):
     v = to_bf16(normal_raster(5502, 1, dims, 2, d))
     out, lse, rel, info = _parity(q, k, v, dims, (3, 9, 17), (1, 1, 1), tol_lse=1e-2 * amp)
     assert rel < 1.5e-2, info
+
+
+def test_without_lse_and_on_a_side_stream():
+    """lse = NULL writes the same out; the call runs on the stream it is given."""
+    from dimensional_sparse_attention_gna_b300 import gna as G
+    dims, window, stride, d = (4, 16, 24), (3, 9, 11), (1, 2, 3), 64
+    q, k, v = bf16_inputs(5600, 1, dims, 2, d)
+    out_ref, lse_ref = gpu_gna(q, k, v, dims, window, stride)
+    dev = torch.device("cuda")
+    B, heads = 1, 2
+    shp = G.tiled_shape(B, heads, dims, d)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        qt, kt = (torch.empty(shp, dtype=torch.bfloat16, device=dev) for _ in range(2))
+        vt = torch.empty(G.value_shape(B, heads, dims, d), dtype=torch.bfloat16, device=dev)
+        G.gna_permute(q.to(dev), qt, B, heads, dims, d, stream=side)
+        G.gna_permute(k.to(dev), kt, B, heads, dims, d, stream=side)
+        G.gna_permute_v(v.to(dev), vt, B, heads, dims, d, stream=side)
+        out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
+        G.gna_forward(qt, kt, vt, out_t, None, B, heads, dims, window, stride, d, stream=side)
+        out = torch.empty((B,) + dims + (heads, d), dtype=torch.bfloat16, device=dev)
+        G.gna_unpermute(out_t, out, B, heads, dims, d, stream=side)
+    side.synchronize()
+    G.gna_get_status(side)
+    np.testing.assert_array_equal(out.float().cpu().numpy(), out_ref)
