@@ -110,7 +110,8 @@ struct Barriers {
     uint64_t q_full;
     uint64_t k_full[4], k_empty[4], v_full[4], v_empty[4];
     uint64_t s_full[2], p_full[2];
-    uint64_t o_done;
+    uint64_t o_done;             // one phase per P V product (rescale waits)
+    uint64_t o_final;            // one phase: the last P V product (epilogue wait)
     uint64_t drain;
 };
 
@@ -307,7 +308,7 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha)
 
 // TT, TH, TW: the layout tile when known at compile time (the default tiles),
 // or 0, 0, 0 for any tile (runtime shape, slower mask construction).
-template <int D, int ESZ, int NS, int TT, int TH, int TW>
+template <int D, int ESZ, int NS, int TT, int TH, int TW, bool RASTER>
 __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_constant__ FwdParams p)
 {
     using C = Cfg<D, ESZ, NS>;
@@ -339,6 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     }
     const int n_kv = box.cnt[0] * box.cnt[1] * box.cnt[2];
     const int64_t kv_row_base = bh * p.tiles_per_head * kTileElems;
+    const int b_idx = static_cast<int>(bh / p.heads);          // batch and head of this CTA
+    const int h_idx = static_cast<int>(bh % p.heads);
 
     const uint32_t sK = smem_u32(smem + C::kSmemK);
     const uint32_t sV = smem_u32(smem + C::kSmemV);
@@ -358,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             mbar_init(bar(bars.p_full[s]), kSoftmaxWarps);
         }
         mbar_init(bar(bars.o_done), 1);
+        mbar_init(bar(bars.o_final), 1);
         mbar_init(bar(bars.drain), 1);
         fence_mbarrier_init();
     }
@@ -395,9 +399,18 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             if (elect_one_sync()) {
                 mbar_arrive_expect_tx(bar(bars.k_full[s]), C::kTileBytes);
 #pragma unroll
-                for (int c = 0; c < C::kChunks; ++c)
-                    tma_load_2d(sK + s * C::kTileBytes + c * kTileElems * C::kRowBytes, &p.tmK, bar(bars.k_full[s]),
-                                c * C::kChunkElems, row);
+                for (int c = 0; c < C::kChunks; ++c) {
+                    const uint32_t dst = sK + s * C::kTileBytes + c * kTileElems * C::kRowBytes;
+                    if constexpr (RASTER) {
+                        // the tile's 128 tokens of this head straight from the raster
+                        // layout: the box (t, y, x) lands in tile element order,
+                        // positions past the grid read as zero
+                        tma_load_5d(dst, &p.tmK, bar(bars.k_full[s]), h_idx * D + c * C::kChunkElems,
+                                    kc[2] * p.tile[2], kc[1] * p.tile[1], kc[0] * p.tile[0], b_idx);
+                    } else {
+                        tma_load_2d(dst, &p.tmK, bar(bars.k_full[s]), c * C::kChunkElems, row);
+                    }
+                }
             }
             __syncwarp();
             ++k_issued;
@@ -451,6 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                     else mma_f8_ts(tO, tP + kk * 8, d, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(bars.o_done));
+                if (i == n_kv - 1) mma_commit(bar(bars.o_final));
                 if (i + NS < n_kv) mma_commit(bar(bars.v_empty[s]));
             }
             __syncwarp();
@@ -500,16 +514,34 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t pair_bar = 1 + quarter;            // named barrier of the two warps sharing these rows
 
-        // Q row -> TMEM (A operand of S = Q K^T)
+        // query coordinates of this row
+        int qpos[3], st[3];
+        {
+            const int ix = row & (p.tile[2] - 1);
+            const int iy = (row >> p.tlog[2]) & (p.tile[1] - 1);
+            const int it = row >> (p.tlog[1] + p.tlog[2]);
+            qpos[0] = qc[0] * p.tile[0] + it;
+            qpos[1] = qc[1] * p.tile[1] + iy;
+            qpos[2] = qc[2] * p.tile[2] + ix;
+        }
+        const bool row_valid = qpos[0] < p.dims[0] && qpos[1] < p.dims[1] && qpos[2] < p.dims[2];
+        // row of this query in the tensor q / out / lse are stored in
+        const int64_t io_row = RASTER
+            ? (((static_cast<int64_t>(b_idx) * p.dims[0] + qpos[0]) * p.dims[1] + qpos[1]) * p.dims[2] + qpos[2]) *
+                      p.heads + h_idx
+            : q_tile_global * kTileElems + row;
+
+        // Q row -> TMEM (A operand of S = Q K^T); padding rows of the raster
+        // layout do not exist and are zero
         {
             constexpr int W = C::kQHalfWords;
             const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const uint8_t*>(p.q) + (q_tile_global * kTileElems + row) * C::kRowBytesAll +
-                half * (C::kRowBytesAll / 2));
+                static_cast<const uint8_t*>(p.q) + io_row * C::kRowBytesAll + half * (C::kRowBytesAll / 2));
+            const bool load = row_valid || !RASTER;
             uint32_t qw[W];
 #pragma unroll
             for (int i = 0; i < W / 4; ++i) {
-                const uint4 v = __ldg(src + i);
+                const uint4 v = load ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
                 qw[4 * i] = v.x;
                 qw[4 * i + 1] = v.y;
                 qw[4 * i + 2] = v.z;
@@ -522,17 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             if (lane == 0) mbar_arrive(bar(bars.q_full));
         }
 
-        // query coordinates of this row and its window starts
-        int qpos[3], st[3];
-        {
-            const int ix = row & (p.tile[2] - 1);
-            const int iy = (row >> p.tlog[2]) & (p.tile[1] - 1);
-            const int it = row >> (p.tlog[1] + p.tlog[2]);
-            qpos[0] = qc[0] * p.tile[0] + it;
-            qpos[1] = qc[1] * p.tile[1] + iy;
-            qpos[2] = qc[2] * p.tile[2] + ix;
-        }
-        const bool row_valid = qpos[0] < p.dims[0] && qpos[1] < p.dims[1] && qpos[2] < p.dims[2];
+        // window starts of this query
 #pragma unroll
         for (int d = 0; d < 3; ++d) st[d] = window_start(qpos[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
 
@@ -659,7 +681,10 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                 m_run = m_new;
                 l_run *= alpha;
                 if (j > 0) {
-                    // O holds PV(0..j-1): wait for PV(j-1), then rescale this half's columns
+                    // O holds PV(0..j-1): wait for PV(j-1), then rescale this half's
+                    // columns.  S(j) has arrived, so every MMA issued before QK(j),
+                    // PV(j-2) included, is complete: o_done is at most one phase
+                    // behind and the parity wait is exact.
                     ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_done), (j - 1) & 1, &abort_flag));
                     if (!ok) {
                         raise_status(&abort_flag);
@@ -705,7 +730,10 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
 
         // ------------------------------------------------------------ epilogue
         if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_done), (n_kv - 1) & 1, &abort_flag));
+            // A parity wait on o_done could pass here while the barrier is
+            // still two phases behind (P V of the second-to-last tile not yet
+            // done): the last product has a barrier of its own.
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_final), 0, &abort_flag));
             if (!ok) raise_status(&abort_flag);
         }
         // every thread of the pair reaches this exchange (even on failure)
@@ -716,7 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             tc_fence_after();
             const bool has = row_valid && l_tot > 0.0f;
             const float inv_l = has ? out_scale / l_tot : 0.0f;
-            uint8_t* out_row = static_cast<uint8_t*>(p.out) + (q_tile_global * kTileElems + row) * (D * 2) + half * D;
+            uint8_t* out_row = static_cast<uint8_t*>(p.out) + io_row * (D * 2) + half * D;
+            const bool store = row_valid || !RASTER;
             // this half of the O row in one TMEM load (16, 32 or 64 columns)
             uint32_t r[C::kOHalf];
             tmem_ld_n<C::kOHalf>(t_ohalf, r);
@@ -731,13 +760,15 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                                                              __uint_as_float(r[c + 2 * i + 1]) * inv_l);
                     pk[i] = *reinterpret_cast<uint32_t*>(&h);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(out_row + c * 2);
-                dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                if (store) {
+                    uint4* dst = reinterpret_cast<uint4*>(out_row + c * 2);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
             }
-            if (p.lse != nullptr && half == 0) {
+            if (p.lse != nullptr && half == 0 && store) {
                 const float lse = has ? (m_run - kShift + __log2f(l_tot)) * kLn2 : -INFINITY;
-                p.lse[q_tile_global * kTileElems + row] = lse;
+                p.lse[io_row] = lse;
             }
         }
     }
@@ -751,14 +782,14 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     }
 }
 
-template <int D, int ESZ, int NS, int TT, int TH, int TW>
+template <int D, int ESZ, int NS, int TT, int TH, int TW, bool RASTER>
 cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
     using C = Cfg<D, ESZ, NS>;
     static_assert(NS <= 4, "barrier arrays hold 4 stages");
     static_assert(C::kSmemAlloc <= 232448 - 4096, "shared memory budget");
     static_assert(C::kQHalfWords == 8 || C::kQHalfWords == 16 || C::kQHalfWords == 32, "Q half-row width");
-    auto kern = gna_fwd_kernel<D, ESZ, NS, TT, TH, TW>;
+    auto kern = gna_fwd_kernel<D, ESZ, NS, TT, TH, TW, RASTER>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     kern<<<dim3(static_cast<unsigned>(num_q_tiles)), kThreads, C::kSmemAlloc, stream>>>(p);
@@ -766,13 +797,23 @@ cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t st
 }
 
 // Default tiles get a kernel with the tile shape compiled in.
+template <int D, int ESZ, int NS, bool RASTER>
+cudaError_t launch_layout(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
+{
+    if (p.tile[0] == 2 && p.tile[1] == 8 && p.tile[2] == 8)
+        return launch_tile<D, ESZ, NS, 2, 8, 8, RASTER>(p, num_q_tiles, stream);
+    if (p.tile[0] == 1 && p.tile[1] == 8 && p.tile[2] == 16)
+        return launch_tile<D, ESZ, NS, 1, 8, 16, RASTER>(p, num_q_tiles, stream);
+    return launch_tile<D, ESZ, NS, 0, 0, 0, RASTER>(p, num_q_tiles, stream);
+}
+
+// The raster layout of q, k, out and lse is a separate kernel, so the tiled
+// path carries none of its addressing.
 template <int D, int ESZ, int NS>
 cudaError_t launch_impl(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
-    if (p.tile[0] == 2 && p.tile[1] == 8 && p.tile[2] == 8) return launch_tile<D, ESZ, NS, 2, 8, 8>(p, num_q_tiles, stream);
-    if (p.tile[0] == 1 && p.tile[1] == 8 && p.tile[2] == 16)
-        return launch_tile<D, ESZ, NS, 1, 8, 16>(p, num_q_tiles, stream);
-    return launch_tile<D, ESZ, NS, 0, 0, 0>(p, num_q_tiles, stream);
+    return p.raster ? launch_layout<D, ESZ, NS, true>(p, num_q_tiles, stream)
+                    : launch_layout<D, ESZ, NS, false>(p, num_q_tiles, stream);
 }
 
 }  // namespace
