@@ -166,6 +166,34 @@ gna_status make_tile_map(CUtensorMap* map, const void* ptr, int64_t rows, int he
     return GNA_OK;
 }
 
+// 5-D TMA view of a raster tensor [B, T, H, W, heads * head_dim] (innermost
+// last), box = one swizzle span of features x (tW, tH, tT) tokens x 1 batch:
+// the box lands in shared memory in tile element order (t, y, x).
+gna_status make_raster_map(CUtensorMap* map, const void* ptr, int B, const int dims[3], int heads, int head_dim,
+                           int esize, const int tile[3])
+{
+    auto enc = encode_fn();
+    if (enc == nullptr) return fail(GNA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    const int row_bytes = head_dim * esize;
+    const int span = row_bytes >= 128 ? 128 : row_bytes;
+    const CUtensorMapSwizzle sw =
+        span == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : span == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    const cuuint64_t token = static_cast<cuuint64_t>(heads) * row_bytes;     // bytes per (t, y, x) position
+    cuuint64_t gdim[5] = {static_cast<cuuint64_t>(heads) * head_dim, static_cast<cuuint64_t>(dims[2]),
+                          static_cast<cuuint64_t>(dims[1]), static_cast<cuuint64_t>(dims[0]),
+                          static_cast<cuuint64_t>(B)};
+    cuuint64_t gstride[4] = {token, token * dims[2], token * dims[2] * dims[1],
+                             token * dims[2] * dims[1] * dims[0]};
+    cuuint32_t box[5] = {static_cast<cuuint32_t>(span / esize), static_cast<cuuint32_t>(tile[2]),
+                         static_cast<cuuint32_t>(tile[1]), static_cast<cuuint32_t>(tile[0]), 1};
+    cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(map, esize == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+                     const_cast<void*>(ptr), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GNA_ERR_CUDA, "cuTensorMapEncodeTiled (raster) failed (%d)", static_cast<int>(r));
+    return GNA_OK;
+}
+
 // 2-D TMA view of a tensor in the value layout: [tiles * head_dim rows, 128
 // tokens], box = head_dim rows x 128 bytes of tokens.
 gna_status make_value_map(CUtensorMap* map, const void* ptr, int64_t tiles, int head_dim, int esize)
@@ -396,9 +424,11 @@ gna_status gna_plan_tile(const int dims[3], const int window[3], const int strid
     return GNA_OK;
 }
 
-gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
-                          const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
-                          const gna_options* opt, void* stream)
+namespace {
+
+gna_status forward_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
+                        const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
+                        const gna_options* opt, void* stream, bool raster)
 {
     if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
         return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -447,7 +477,14 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out
     if (const char* f = std::getenv("GNA_TEST_SKIP_KV_LOAD")) p.fault_skip_kv = std::atoi(f);
 
     p.q = q;
-    if ((st = make_tile_map(&p.tmK, k, rows, head_dim, es)) != GNA_OK) return st;
+    p.raster = raster ? 1 : 0;
+    if (raster) {
+        if (static_cast<int64_t>(B) * dims[0] > INT32_MAX || static_cast<int64_t>(heads) * head_dim > INT32_MAX)
+            return fail(GNA_ERR_UNSUPPORTED, "raster tensor too large for TMA coordinates");
+        if ((st = make_raster_map(&p.tmK, k, B, dims, heads, head_dim, es, p.tile)) != GNA_OK) return st;
+    } else if ((st = make_tile_map(&p.tmK, k, rows, head_dim, es)) != GNA_OK) {
+        return st;
+    }
     if ((st = make_value_map(&p.tmV, v, num_q_tiles, head_dim, es)) != GNA_OK) return st;
 
     cudaError_t e = gna::launch_forward(p, head_dim, es, num_q_tiles, static_cast<cudaStream_t>(stream));
@@ -457,11 +494,27 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out
     return GNA_OK;
 }
 
+}  // namespace
+
+gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
+                          const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
+                          const gna_options* opt, void* stream)
+{
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, false);
+}
+
 gna_status gna_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
                        const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
                        void* stream)
 {
-    return gna_forward_ex(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, nullptr, stream);
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, nullptr, stream, false);
+}
+
+gna_status gna_forward_raster(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
+                              const int dims[3], const int window[3], const int stride[3], int head_dim,
+                              gna_dtype dtype, const gna_options* opt, void* stream)
+{
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, true);
 }
 
 gna_status gna_get_status(void* stream)

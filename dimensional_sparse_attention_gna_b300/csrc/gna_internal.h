@@ -29,9 +29,11 @@ cudaError_t launch_permute_v(const void* src, void* dst, const PermuteGeom& g, i
 
 // Parameters of one attention launch (passed by value as a __grid_constant__).
 struct FwdParams {
-    CUtensorMap tmK;             // 2-D TMA view [rows, head_dim] of the tiled k
+    CUtensorMap tmK;             // 2-D TMA view [rows, head_dim] of the tiled k, or (raster) the
+                                 // 5-D view [B, T, H, W, heads * head_dim] of the raster k
     CUtensorMap tmV;             // 2-D TMA view [rows * head_dim / 128, 128] of v in the value layout
-    const void* q;               // tiled q [rows, head_dim] (read row by row into TMEM)
+    const void* q;               // tiled q [rows, head_dim], or raster q (read row by row into TMEM)
+    int raster;                  // 1: q, k, out and lse use the raster layout (v stays in the value layout)
     void* out;                   // tiled bf16 [rows, head_dim]
     float* lse;                  // tiled float [rows] or nullptr
     const float* descale;        // e4m3 only: 3 device floats (q, k, v) or nullptr

@@ -91,6 +91,8 @@ def lib() -> ctypes.CDLL:
         L.gna_forward_ex.restype = st
         L.gna_forward_ex.argtypes = [_P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _INT,
                                      ctypes.POINTER(GNAOptions), _P]
+        L.gna_forward_raster.restype = st
+        L.gna_forward_raster.argtypes = L.gna_forward_ex.argtypes
         L.gna_tile_stats.restype = st
         L.gna_tile_stats.argtypes = [_I3, _I3, _I3, _P, _INT, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
@@ -254,6 +256,36 @@ def gna_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Te
                                   _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
                                   _stream_ptr(stream))
     _check(st)
+
+
+def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                       lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int, *,
+                       tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0,
+                       descale: torch.Tensor | None = None, stream=None):
+    """GNA forward with q, k, out and lse in the raster layout (see ``include/gna.h``).
+
+    ``q, k``: bf16 or float8_e4m3fn ``[B, T, H, W, heads, head_dim]``; ``v``:
+    same dtype, value layout (:func:`gna_permute_v` with the same ``tile``);
+    ``out``: bf16 raster; ``lse``: float32 ``[B, T, H, W, heads]`` or None.
+    """
+    code = dtype_code(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if out.dtype != torch.bfloat16:
+        raise ValueError("out must be bfloat16")
+    if lse is not None and lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    opt = GNAOptions()
+    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+    opt.leader_rule = leader_rule
+    opt.scale = scale
+    if descale is not None:
+        if descale.dtype != torch.float32 or descale.numel() != 3:
+            raise ValueError("descale must be 3 float32 values")
+        opt.descale = _ptr(descale)
+    _check(lib().gna_forward_raster(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+                                    _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
+                                    _stream_ptr(stream)))
 
 
 def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADER_CENTER):

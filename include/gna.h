@@ -167,6 +167,24 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out
                           int B, int heads, const int dims[3], const int window[3], const int stride[3],
                           int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
 
+/* gna_forward_ex without the tiled permutes of Q, K, O and lse.  The same
+ * arithmetic on the same tiles (GNA page §2.1: the multi-dimensional tiling is
+ * a view of the token grid); the kernel gathers each 128-token Q and K tile
+ * straight from the raster tensors, a 5-D TMA box for K and row loads for Q,
+ * and writes O and lse back to raster rows.  Query rows of padded tile slots
+ * are neither read nor written.
+ *
+ * q, k    : raster [B, T, H, W, heads, head_dim], row stride heads*head_dim
+ * v       : value layout [B, heads, tiles, head_dim, 128] (gna_permute_v_tiled
+ *           with the same tile)
+ * out     : raster [B, T, H, W, heads, head_dim] bfloat16
+ * lse     : raster [B, T, H, W, heads] float32, natural log; may be NULL
+ * Everything else as gna_forward_ex; opt may be NULL.  All pointers 16-byte
+ * aligned.  GNA_ERR_INVALID_ARG / GNA_ERR_UNSUPPORTED as gna_forward_ex. */
+gna_status gna_forward_raster(const void* q, const void* k, const void* v, void* out, float* lse,
+                              int B, int heads, const int dims[3], const int window[3], const int stride[3],
+                              int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
+
 /* ------------------------------------------------------------ planning ---- */
 
 /* Tile statistics of one (b, head) plane under the given tile (NULL =

@@ -87,6 +87,16 @@ def test_forward_ex_rejects_bad_options(L):
         assert L.gna_forward_ex(*args, ctypes.byref(opt), None) == G.GNA_ERR_INVALID_ARG
 
 
+def test_forward_raster_rejects_bad_arguments_on_host(L):
+    args = (1, 2, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1), 32, G.GNA_BF16, None, None)
+    assert L.gna_forward_raster(None, FAKE, FAKE, FAKE, None, *args) == G.GNA_ERR_INVALID_ARG
+    assert L.gna_forward_raster(FAKE, FAKE + 8, FAKE, FAKE, None, *args) == G.GNA_ERR_INVALID_ARG
+    bad_geom = (1, 2, I3(1, 16, 16), I3(1, 17, 5), I3(1, 1, 1), 32, G.GNA_BF16, None, None)
+    assert L.gna_forward_raster(FAKE, FAKE, FAKE, FAKE, None, *bad_geom) == G.GNA_ERR_INVALID_ARG
+    bad_d = (1, 2, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1), 96, G.GNA_BF16, None, None)
+    assert L.gna_forward_raster(FAKE, FAKE, FAKE, FAKE, None, *bad_d) == G.GNA_ERR_UNSUPPORTED
+
+
 def test_permute_rejects_bad_arguments_on_host(L):
     assert L.gna_permute(None, FAKE, 1, 1, I3(1, 4, 4), 8, G.GNA_BF16, None) == G.GNA_ERR_INVALID_ARG
     assert L.gna_permute(FAKE, FAKE + 4, 1, 1, I3(1, 4, 4), 8, G.GNA_BF16, None) == G.GNA_ERR_INVALID_ARG
