@@ -4,7 +4,8 @@ One step = one pass of the whole path over one batch of synthetic input:
     permute Q, K (raster -> 128-token tiles) and V (-> feature-major tiles)
     ->  fused GNA forward
     ->  unpermute O and lse (tiles -> raster)
-on the 720p-video latent workload (30 x 48 x 80 tokens, 24 heads, head_dim 128,
+or, with ``--layout raster``, permute V -> the forward reading Q, K and
+writing O, lse in the raster layout, on the 720p-video latent workload (30 x 48 x 80 tokens, 24 heads, head_dim 128,
 window 16 x 32 x 48, bf16), the configuration the GNA page's video results and
 its Blackwell kernel throughput are about.
 
@@ -54,6 +55,9 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"])
+    ap.add_argument("--layout", default="tiled", choices=["tiled", "raster"],
+                    help="tiled: permute Q, K, V and unpermute O, lse around gna_forward; "
+                         "raster: permute V only, gna_forward_raster on raster Q, K, O, lse")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--sustain", type=float, default=0.0,
@@ -88,9 +92,10 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_traffic(per_unit_heads: int, heads: int, B: int):
+def kernel_traffic(per_unit_heads: int, heads: int, B: int, layout: str = "tiled"):
     """DRAM bytes per forward launch from the committed ncu capture, scaled to this
-    launch by (b, head) planes, or None if the kernel source changed since."""
+    launch by (b, head) planes, or None if the kernel source changed since (or the
+    capture is of the other layout's kernel)."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -98,7 +103,7 @@ def kernel_traffic(per_unit_heads: int, heads: int, B: int):
             h = hashlib.sha256(f.read()).hexdigest()
     except OSError:
         return None
-    if rec.get("source_sha256") != h:
+    if rec.get("source_sha256") != h or rec.get("layout", "tiled") != layout:
         return None
     return rec["bytes_per_plane"] * heads * B
 
@@ -304,36 +309,54 @@ def gpu_arm(a, rank, world, local):
             descale = (descale or []) + [s]
         del x
     ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)
+    raster = a.layout == "raster"
     shp = G.tiled_shape(B, heads, dims, d)
-    qt, kt = (torch.empty(shp, dtype=dt, device=dev) for _ in range(2))
+    if not raster:                      # the raster path has no tiled Q, K, O or lse
+        qt, kt = (torch.empty(shp, dtype=dt, device=dev) for _ in range(2))
+        out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
+        lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     vt = torch.empty(G.value_shape(B, heads, dims, d), dtype=dt, device=dev)
-    out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
-    lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     out = torch.empty(raster_shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(raster_shape[:-1] + (1,), dtype=torch.float32, device=dev)
 
-    ev = {"fwd": [], "perm": []}
+    def forward(window, stride, q_in, k_in, o_dst, lse_dst):
+        """One forward launch of the bench's layout (raster tensors in, raster out)."""
+        if raster:
+            G.gna_forward_raster(q_in, k_in, vt, o_dst, lse_dst[..., 0], B, heads, dims, window, stride, d,
+                                 descale=ds, stream=stream)
+        else:
+            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, window, stride, d, descale=ds, stream=stream)
+
+    def permute_in(q_in, k_in, v_in):
+        if not raster:
+            G.gna_permute(q_in, qt, B, heads, dims, d, stream=stream)
+            G.gna_permute(k_in, kt, B, heads, dims, d, stream=stream)
+        G.gna_permute_v(v_in, vt, B, heads, dims, d, stream=stream)
+
+    def unpermute_out(o_dst, lse_dst):
+        if not raster:
+            G.gna_unpermute(out_t, o_dst, B, heads, dims, d, stream=stream)
+            G.gna_unpermute(lse_t.unsqueeze(-1), lse_dst, B, heads, dims, 1, stream=stream)
+
+    ev = {"fwd": [], "perm": [], "unperm": []}
 
     def step(record=False):
         if record:
             e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
             e[0].record(stream)
-        G.gna_permute(xs[0], qt, B, heads, dims, d, stream=stream)
-        G.gna_permute(xs[1], kt, B, heads, dims, d, stream=stream)
-        G.gna_permute_v(xs[2], vt, B, heads, dims, d, stream=stream)
+        permute_in(*xs)
         if record:
             e[1].record(stream)
-        G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds, stream=stream)
+        forward(a.window, a.stride, xs[0], xs[1], out, lse)
         if record:
             e[2].record(stream)
-        G.gna_unpermute(out_t, out, B, heads, dims, d, stream=stream)
-        G.gna_unpermute(lse_t.unsqueeze(-1), lse, B, heads, dims, 1, stream=stream)
+        unpermute_out(out, lse)
         if record:
             e[3].record(stream)
             ev["perm"].append((e[0], e[1]))
             ev["fwd"].append((e[1], e[2]))
-            ev.setdefault("unperm", []).append((e[2], e[3]))
-    launches_per_step = 6
+            ev["unperm"].append((e[2], e[3]))
+    launches_per_step = 2 if raster else 6
 
     for _ in range(a.warmup):
         step()
@@ -367,8 +390,8 @@ def gpu_arm(a, rank, world, local):
     value = total_flops / (elapsed_ms / 1e3) / 1e12
     kernel_tflops = flops_rank / (fwd_ms / 1e3) / 1e12
     esz = torch.tensor([], dtype=dt).element_size()
-    perm_bytes = 3 * 2 * B * math.prod(dims) * heads * d * esz
-    unperm_bytes = 2 * B * math.prod(dims) * heads * (d * 2 + 4)
+    perm_bytes = (1 if raster else 3) * 2 * B * math.prod(dims) * heads * d * esz
+    unperm_bytes = 0 if raster else 2 * B * math.prod(dims) * heads * (d * 2 + 4)
 
     peaks, peaks_kind = load_peaks()
     # Denominators: the measured cuBLAS bf16 GEMM rates (fp8 takes twice the
@@ -387,13 +410,12 @@ def gpu_arm(a, rank, world, local):
     speedup = None
     dense_ms = None
     if not a.no_dense:
-        for _ in range(1):
-            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, dims, (1, 1, 1), d, descale=ds, stream=stream)
+        forward(dims, (1, 1, 1), xs[0], xs[1], out, lse)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         reps = 2
         e0.record(stream)
         for _ in range(reps):
-            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, dims, (1, 1, 1), d, descale=ds, stream=stream)
+            forward(dims, (1, 1, 1), xs[0], xs[1], out, lse)
         e1.record(stream)
         torch.cuda.synchronize()
         G.gna_get_status(stream)
@@ -401,8 +423,8 @@ def gpu_arm(a, rank, world, local):
         speedup = dense_ms / fwd_ms
 
     # end to end through the public API with host buffers: every step copies its
-    # Q, K, V from pinned host memory, runs permute -> forward -> unpermute and
-    # copies O and lse back.  Copies run on their own streams so that step k+1's
+    # Q, K, V from pinned host memory, runs the step's kernels and copies O and
+    # lse back.  Copies run on their own streams so that step k+1's
     # upload and step k-1's download overlap step k's kernels (two buffer sets).
     e2e = None
     if not a.no_e2e:
@@ -425,17 +447,16 @@ def gpu_arm(a, rank, world, local):
                     dv.copy_(h, non_blocking=True)
             ev["in_ready"][b].record(s_in)
             stream.wait_event(ev["in_ready"][b])
-            G.gna_permute(dev_in[b][0], qt, B, heads, dims, d, stream=stream)
-            G.gna_permute(dev_in[b][1], kt, B, heads, dims, d, stream=stream)
-            G.gna_permute_v(dev_in[b][2], vt, B, heads, dims, d, stream=stream)
-            ev["perm_done"][b].record(stream)
-            used["perm_done"][b] = True
-            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds,
-                          stream=stream)
+            permute_in(*dev_in[b])
+            if not raster:
+                ev["perm_done"][b].record(stream)
             if used["out_done"][b]:
                 stream.wait_event(ev["out_done"][b])      # results of step k-2 downloaded
-            G.gna_unpermute(out_t, dev_out[b], B, heads, dims, d, stream=stream)
-            G.gna_unpermute(lse_t.unsqueeze(-1), dev_lse[b], B, heads, dims, 1, stream=stream)
+            forward(a.window, a.stride, dev_in[b][0], dev_in[b][1], dev_out[b], dev_lse[b])
+            if raster:
+                ev["perm_done"][b].record(stream)         # the forward read the raster Q, K
+            used["perm_done"][b] = True
+            unpermute_out(dev_out[b], dev_lse[b])
             ev["comp_done"][b].record(stream)
             s_out.wait_event(ev["comp_done"][b])
             with torch.cuda.stream(s_out):
@@ -477,8 +498,7 @@ def gpu_arm(a, rank, world, local):
             s0.record(stream)
             while time.time() - t_wall < a.sustain:
                 for _ in range(5):
-                    G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, descale=ds,
-                                  stream=stream)
+                    forward(a.window, a.stride, xs[0], xs[1], out, lse)
                 n_sus += 5
                 stream.synchronize()
             s1.record(stream)
@@ -488,7 +508,7 @@ def gpu_arm(a, rank, world, local):
         sustained = {"value": flops_rank / (sus_ms / 1e3) / 1e12, "unit": "TFLOP/s", "launches": n_sus,
                      "forward_ms": sus_ms, "seconds": a.sustain, "clocks": sclk.summary(),
                      "frac_of_sustained_peak": flops_rank / (sus_ms / 1e3) / 1e12 / peak_sustained}
-    traffic = kernel_traffic(1, heads, B)
+    traffic = kernel_traffic(1, heads, B, a.layout)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
@@ -508,7 +528,7 @@ def gpu_arm(a, rank, world, local):
         "data": "synthetic: iid N(0,1) Q/K/V drawn on the device per rank",
         "config": {"workload": workload_name(a), "dims": list(dims), "window": list(a.window),
                    "stride": list(a.stride), "heads": heads, "B": B, "head_dim": d,
-                   "tile": list(G.gna_tile_shape(dims)),
+                   "tile": list(G.gna_tile_shape(dims)), "layout": a.layout,
                    "l2": "inputs larger than L2 (3 x %.0f MB raster + tiled copies)" % (
                        B * math.prod(dims) * heads * d * esz / 1e6),
                    "parallelism": f"replicas x{world}: every rank runs the full workload on its own data"},
@@ -518,10 +538,11 @@ def gpu_arm(a, rank, world, local):
                      "frac_of_sustained_peak": kernel_tflops / peak_sustained,
                      "tile_work_tflops": tile_flops / (fwd_ms / 1e3) / 1e12,
                      "tile_overhead": tile_flops / flops_rank, "partial_tile_share": partial / visited},
-        "kernels_ms": {"permute_qkv": perm_ms, "forward": fwd_ms, "unpermute_o_lse": unperm_ms},
+        "kernels_ms": {("permute_v" if raster else "permute_qkv"): perm_ms, "forward": fwd_ms,
+                       "unpermute_o_lse": None if raster else unperm_ms},
         "permute_gbps": perm_bytes / (perm_ms / 1e3) / 1e9,
         "permute_frac_of_hbm": perm_bytes / (perm_ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6400.0),
-        "unpermute_gbps": unperm_bytes / (unperm_ms / 1e3) / 1e9,
+        "unpermute_gbps": None if raster else unperm_bytes / (unperm_ms / 1e3) / 1e9,
         "dense_forward_ms": dense_ms, "speedup_vs_dense": speedup,
         "flop_sparsity_ratio": n_ratio,
         "speedup_bound_at_equal_tile_rate": G.gna_plan_tile(dims, a.window, a.stride)[2],

@@ -20,11 +20,16 @@
 //               halves of a row swap their partial maxima through shared
 //               memory once per tile; row sums stay partial until the end.
 // TMEM (512 columns): O [0, 128), S double buffer [128, 256) and [256, 384),
-// Q [384, 384 + head_dim * elem / 4).  Q sits in TMEM so S = Q K^T reads only
-// K from shared memory; P overwrites the front of its S buffer (bf16: 64
-// columns, e4m3: 32) and feeds O += P V straight from TMEM.  V comes in the
-// value layout (each tile feature-major), so both MMAs read their shared-memory
-// operand K-major.
+// Q [384, 384 + head_dim * elem / 4), and for e4m3 a P double buffer [448,
+// 512).  Q sits in TMEM so S = Q K^T reads only K from shared memory; P feeds
+// O += P V straight from TMEM.  bf16 P (64 columns) has no room of its own
+// and overwrites the front of its S buffer, so QK(j + 2) writes columns that
+// PV(j), an MMA on another accumulator issued just before it, reads: the
+// kernel relies on the tensor core executing MMAs in issue order.  e4m3 P
+// (32 columns) sits in buffers of its own and needs no such ordering: P(j)
+// is written after S(j) arrived, so PV(j - 2), the last reader of its buffer,
+// is complete.  V comes in the value layout (each tile feature-major), so both
+// MMAs read their shared-memory operand K-major.
 // MMA issue order  QK(0) QK(1) PV(0) QK(2) PV(1) ...  keeps the tensor core on
 // the next S while the softmax warps work on the current one.
 //
@@ -59,6 +64,15 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;
 constexpr uint32_t kColS0 = 128;
 constexpr uint32_t kColQ = 384;
+constexpr uint32_t kColP8 = 448;       // e4m3: P double buffer [448, 480) and [480, 512)
+
+// TMEM column of P(j) in buffer b = j & 1: bf16 P (64 columns) overwrites the
+// front of S buffer b; e4m3 P (32 columns) has two buffers of its own.
+template <int ESZ>
+__device__ __forceinline__ uint32_t p_col(int b)
+{
+    return ESZ == 1 ? kColP8 + static_cast<uint32_t>(b) * 32 : kColS0 + static_cast<uint32_t>(b) * 128;
+}
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -454,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             tc_fence_after();
             if (elect_one_sync()) {
                 const uint64_t dv = dV0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
-                const uint32_t tP = tmem + kColS0 + (i & 1) * 128;
+                const uint32_t tP = tmem + p_col<ESZ>(i & 1);
 #pragma unroll
                 for (int kk = 0; kk < C::kPVSteps; ++kk) {
                     // k-step kk covers tokens [kk * K, kk * K + K): 32 bytes of every feature row
@@ -720,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             {
                 uint32_t pk[C::kPHalfWords];
                 pack_p<ESZ>(s, pk);
-                tmem_store_n<C::kPHalfWords>(t_s + half * C::kPHalfWords, pk);
+                tmem_store_n<C::kPHalfWords>(tmem + p_col<ESZ>(sb) + lane_addr + half * C::kPHalfWords, pk);
                 tmem_wait_st();
             }
             tc_fence_before();
@@ -789,6 +803,8 @@ cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t st
     static_assert(NS <= 4, "barrier arrays hold 4 stages");
     static_assert(C::kSmemAlloc <= 232448 - 4096, "shared memory budget");
     static_assert(C::kQHalfWords == 8 || C::kQHalfWords == 16 || C::kQHalfWords == 32, "Q half-row width");
+    static_assert(ESZ == 2 || (kColQ + 2 * C::kQHalfWords <= kColP8 && kColP8 + 4 * C::kPHalfWords <= kTmemCols),
+                  "TMEM columns of the e4m3 P buffers");
     auto kern = gna_fwd_kernel<D, ESZ, NS, TT, TH, TW, RASTER>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
