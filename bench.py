@@ -95,7 +95,7 @@ def load_peaks():
 def kernel_traffic(per_unit_heads: int, heads: int, B: int, layout: str = "tiled"):
     """DRAM bytes per forward launch from the committed ncu capture, scaled to this
     launch by (b, head) planes, or None if the kernel source changed since (or the
-    capture is of the other layout's kernel)."""
+    layout's kernel was not captured)."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -103,9 +103,9 @@ def kernel_traffic(per_unit_heads: int, heads: int, B: int, layout: str = "tiled
             h = hashlib.sha256(f.read()).hexdigest()
     except OSError:
         return None
-    if rec.get("source_sha256") != h or rec.get("layout", "tiled") != layout:
+    if rec.get("source_sha256") != h or layout not in rec.get("layouts", {}):
         return None
-    return rec["bytes_per_plane"] * heads * B
+    return rec["layouts"][layout]["bytes_per_plane"] * heads * B
 
 
 # ------------------------------------------------------------------ distributed plumbing
