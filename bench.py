@@ -92,10 +92,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_traffic(per_unit_heads: int, heads: int, B: int, layout: str = "tiled"):
+def kernel_traffic(a) -> int | None:
     """DRAM bytes per forward launch from the committed ncu capture, scaled to this
-    launch by (b, head) planes, or None if the kernel source changed since (or the
-    layout's kernel was not captured)."""
+    launch by (b, head) planes; None unless the workload (grid, window, stride,
+    head_dim, dtype) and layout are the captured ones and the kernel source is
+    unchanged since the capture."""
     try:
         with open(TRAFFIC_FILE) as f:
             rec = json.load(f)
@@ -103,9 +104,12 @@ def kernel_traffic(per_unit_heads: int, heads: int, B: int, layout: str = "tiled
             h = hashlib.sha256(f.read()).hexdigest()
     except OSError:
         return None
-    if rec.get("source_sha256") != h or layout not in rec.get("layouts", {}):
+    m = rec.get("match", {})
+    same = (list(a.dims) == m.get("dims") and list(a.window) == m.get("window") and list(a.stride) == m.get("stride")
+            and a.head_dim == m.get("head_dim") and a.dtype == m.get("dtype"))
+    if rec.get("source_sha256") != h or not same or a.layout not in rec.get("layouts", {}):
         return None
-    return rec["layouts"][layout]["bytes_per_plane"] * heads * B
+    return rec["layouts"][a.layout]["bytes_per_plane"] * a.heads * a.batch
 
 
 # ------------------------------------------------------------------ distributed plumbing
@@ -508,7 +512,7 @@ def gpu_arm(a, rank, world, local):
         sustained = {"value": flops_rank / (sus_ms / 1e3) / 1e12, "unit": "TFLOP/s", "launches": n_sus,
                      "forward_ms": sus_ms, "seconds": a.sustain, "clocks": sclk.summary(),
                      "frac_of_sustained_peak": flops_rank / (sus_ms / 1e3) / 1e12 / peak_sustained}
-    traffic = kernel_traffic(1, heads, B, a.layout)
+    traffic = kernel_traffic(a)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:

@@ -81,3 +81,25 @@ def test_reference_arm_prints_one_contract_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_traffic_record_applies_only_to_the_captured_workload():
+    """The committed ncu DRAM bytes scale with (b, head) planes of the captured
+    workload and layout; any other workload reports null rather than a guess."""
+    sys.path.insert(0, ROOT)
+    import bench
+    rec = json.load(open(bench.TRAFFIC_FILE))
+    m = rec["match"]
+    base = ["--dims", ",".join(map(str, m["dims"])), "--window", ",".join(map(str, m["window"])),
+            "--stride", ",".join(map(str, m["stride"])), "--head-dim", str(m["head_dim"]), "--dtype", m["dtype"]]
+    t1 = bench.kernel_traffic(bench.parse_args(base + ["--heads", "1"]))
+    if t1 is None:        # the kernel source changed since the capture: nothing may be reported
+        assert bench.kernel_traffic(bench.parse_args(base)) is None
+        return
+    assert t1 == rec["layouts"]["tiled"]["bytes_per_plane"]
+    assert bench.kernel_traffic(bench.parse_args(base + ["--heads", "6", "--batch", "2"])) == 12 * t1
+    assert bench.kernel_traffic(bench.parse_args(base + ["--heads", "1", "--layout", "raster"])) == \
+        rec["layouts"]["raster"]["bytes_per_plane"]
+    other = "fp8" if m["dtype"] == "bf16" else "bf16"
+    assert bench.kernel_traffic(bench.parse_args(base[:-1] + [other])) is None
+    assert bench.kernel_traffic(bench.parse_args(base + ["--window", "1,1,1"])) is None
