@@ -98,13 +98,16 @@ void default_tile(const int dims[3], int tile[3])
 
 gna_status check_tile(const int tile[3], int tlog[3])
 {
-    int prod = 1;
+    int log_sum = 0;          // log2 of the volume (summed, so no product can overflow)
     for (int d = 0; d < 3; ++d) {
         tlog[d] = ilog2_exact(tile[d]);
         if (tlog[d] < 0) return fail(GNA_ERR_INVALID_ARG, "tile[%d] = %d is not a positive power of two", d, tile[d]);
-        prod *= tile[d];
+        log_sum += tlog[d];
     }
-    if (prod != gna::kTileElems) return fail(GNA_ERR_INVALID_ARG, "tile volume %d != %d", prod, gna::kTileElems);
+    static_assert(gna::kTileElems == 1 << 7, "tile volume is 2^7");
+    if (log_sum != 7)
+        return fail(GNA_ERR_INVALID_ARG, "tile %d x %d x %d does not hold %d elements", tile[0], tile[1], tile[2],
+                    gna::kTileElems);
     return GNA_OK;
 }
 

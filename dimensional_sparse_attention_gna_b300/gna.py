@@ -128,6 +128,24 @@ def _ptr(t: torch.Tensor | None) -> int | None:
     return t.data_ptr()
 
 
+def _raster_elems(B: int, heads: int, dims, head_dim: int) -> int:
+    return B * dims[0] * dims[1] * dims[2] * heads * head_dim
+
+
+def _need(**tensors_and_sizes):
+    """Every tensor must hold at least the elements the call touches (the C ABI
+    takes bare pointers and cannot check), and all must share one device."""
+    devices = set()
+    for name, (t, n) in tensors_and_sizes.items():
+        if t is None:
+            continue
+        if t.numel() < n:
+            raise ValueError(f"{name} holds {t.numel()} elements, the call touches {n}")
+        devices.add(t.device)
+    if len(devices) > 1:
+        raise ValueError(f"tensors on different devices: {sorted(map(str, devices))}")
+
+
 def dtype_code(dtype: torch.dtype) -> int:
     try:
         return _DTYPE_CODES[dtype]
@@ -165,6 +183,8 @@ def gna_permute(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims, 
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
+    _need(src=(src, _raster_elems(B, heads, dims, head_dim)),
+          dst=(dst, gna_tiled_elems(B, heads, dims, head_dim, tile)))
     if tile is None:
         st = lib().gna_permute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
     else:
@@ -179,6 +199,8 @@ def gna_unpermute(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
+    _need(src=(src, gna_tiled_elems(B, heads, dims, head_dim, tile)),
+          dst=(dst, _raster_elems(B, heads, dims, head_dim)))
     if tile is None:
         st = lib().gna_unpermute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
     else:
@@ -199,6 +221,8 @@ def gna_permute_v(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
+    _need(src=(src, _raster_elems(B, heads, dims, head_dim)),
+          dst=(dst, gna_tiled_elems(B, heads, dims, head_dim, tile)))
     if tile is None:
         st = lib().gna_permute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
     else:
@@ -213,6 +237,8 @@ def gna_unpermute_v(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, di
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
+    _need(src=(src, gna_tiled_elems(B, heads, dims, head_dim, tile)),
+          dst=(dst, _raster_elems(B, heads, dims, head_dim)))
     if tile is None:
         st = lib().gna_unpermute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
     else:
@@ -239,6 +265,8 @@ def gna_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Te
         raise ValueError("out must be bfloat16")
     if lse is not None and lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
+    nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
+    _need(q=(q, nt), k=(k, nt), v=(v, nt), out=(out, nt), lse=(lse, nt // head_dim))
     plain = tile is None and leader_rule == GNA_LEADER_CENTER and scale == 0.0 and descale is None
     if plain:
         st = lib().gna_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
@@ -275,6 +303,9 @@ def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: t
         raise ValueError("out must be bfloat16")
     if lse is not None and lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
+    nr = _raster_elems(B, heads, dims, head_dim)
+    _need(q=(q, nr), k=(k, nr), v=(v, gna_tiled_elems(B, heads, dims, head_dim, tile)), out=(out, nr),
+          lse=(lse, nr // head_dim))
     opt = GNAOptions()
     opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
     opt.leader_rule = leader_rule

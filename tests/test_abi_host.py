@@ -79,7 +79,8 @@ def test_forward_rejects_bad_arguments_on_host(L, kwargs, status):
 def test_forward_ex_rejects_bad_options(L):
     args = (FAKE, FAKE, FAKE, FAKE, None, 1, 1, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1), 32, G.GNA_BF16)
     for tile, rule, scale in [((1, 8, 8), 0, 0.0), ((1, 3, 16), 0, 0.0), ((1, 8, 16), 2, 0.0),
-                              ((1, 8, 16), 0, float("nan"))]:
+                              ((1, 8, 16), 0, float("nan")), ((1 << 30, 1 << 30, 1 << 30), 0, 0.0),
+                              ((1 << 28, 1, 1 << 3), 0, 0.0)]:
         opt = G.GNAOptions()
         opt.tile = (ctypes.c_int * 3)(*tile)
         opt.leader_rule = rule
@@ -218,3 +219,35 @@ def test_plan_tile_blocked_aligned_is_exact(L):
     tile, overhead, speedup = G.gna_plan_tile((32, 48, 96), (16, 32, 48), (16, 32, 48))
     assert overhead == 1.0
     assert math.isclose(speedup, 32 * 48 * 96 / (16 * 32 * 48), rel_tol=1e-12)
+
+
+def test_binding_checks_tensor_sizes_before_any_call():
+    """The C ABI takes bare pointers; the binding refuses tensors smaller than
+    what a call touches (checked on the host, before the CUDA-device check)."""
+    import torch
+    B, heads, dims, d = 1, 2, (1, 16, 16), 32
+    nr = B * 16 * 16 * heads * d
+    nt = G.gna_tiled_elems(B, heads, dims, d)
+    bf = torch.bfloat16
+    ok_raster, small_raster = torch.empty(nr, dtype=bf), torch.empty(nr - 1, dtype=bf)
+    ok_tiled, small_tiled = torch.empty(nt, dtype=bf), torch.empty(nt - 1, dtype=bf)
+    with pytest.raises(ValueError, match="dst holds"):
+        G.gna_permute(ok_raster, small_tiled, B, heads, dims, d)
+    with pytest.raises(ValueError, match="src holds"):
+        G.gna_permute_v(small_raster, ok_tiled, B, heads, dims, d)
+    with pytest.raises(ValueError, match="dst holds"):
+        G.gna_unpermute(ok_tiled, small_raster, B, heads, dims, d)
+    with pytest.raises(ValueError, match="out holds"):
+        G.gna_forward(ok_tiled, ok_tiled, ok_tiled, small_tiled, None, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
+    lse_small = torch.empty(nt // d - 1, dtype=torch.float32)
+    with pytest.raises(ValueError, match="lse holds"):
+        G.gna_forward(ok_tiled, ok_tiled, ok_tiled, ok_tiled, lse_small, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
+    with pytest.raises(ValueError, match="q holds"):
+        G.gna_forward_raster(small_raster, ok_raster, ok_tiled, ok_raster, None, B, heads, dims, (1, 5, 5),
+                             (1, 1, 1), d)
+    with pytest.raises(ValueError, match="v holds"):
+        G.gna_forward_raster(ok_raster, ok_raster, small_tiled, ok_raster, None, B, heads, dims, (1, 5, 5),
+                             (1, 1, 1), d)
+    # sizes right: the next refusal is the device check (CPU tensors)
+    with pytest.raises(ValueError, match="CUDA device"):
+        G.gna_forward(ok_tiled, ok_tiled, ok_tiled, ok_tiled, None, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
