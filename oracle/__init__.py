@@ -1,4 +1,4 @@
-"""CPU oracle of the GNA forward pass -- TEST INFRASTRUCTURE ONLY.
+"""CPU oracle of the GNA forward pass and its gradients -- TEST INFRASTRUCTURE ONLY.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package.  The product
@@ -11,9 +11,12 @@ Contents
   query at a time, and the same quantity as masked dense attention).
 * :mod:`oracle.layout`    -- the tile-major layout definition (reshape/transpose).
 * ``gna_oracle.c``        -- the same definition in plain C, threaded over
-  queries, float64 accumulation; wrapped here by :func:`forward_c`.
+  queries, float64 accumulation; wrapped here by :func:`forward_c`; and its
+  derivative (the backward pass), threaded over (b, head) planes, wrapped by
+  :func:`backward_c`.
 
-Every function is pinned by ``tests/test_oracle_pins.py`` against hand-derived
+Every function is pinned by ``tests/test_oracle_pins.py`` (the backward by
+``tests/test_oracle_backward_pins.py``) against hand-derived
 tables, closed forms, special cases that reduce to library routines, brute
 force and invariants.  Parity of the large workloads is checked on sampled
 queries, which this C oracle computes one by one.
@@ -62,6 +65,13 @@ def _load():
                 ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                 ctypes.c_void_p, ctypes.c_int64,
                 ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.gna_oracle_backward.restype = ctypes.c_int
+            lib.gna_oracle_backward.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int,
+                ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.gna_oracle_window_starts.restype = None
             lib.gna_oracle_window_starts.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, ctypes.c_void_p]
@@ -133,3 +143,25 @@ def forward_c(q, k, v, dims, window, stride, scale=None, rule=LEADER_CENTER,
         lse = lse.reshape(B, heads, T, H, W).transpose(0, 2, 3, 4, 1)
         return np.ascontiguousarray(out), np.ascontiguousarray(lse)
     return out, lse
+
+
+def backward_c(q, k, v, dout, dims, window, stride, scale=None, rule=LEADER_CENTER, threads=None):
+    """Run the C backward oracle: ``(dq, dk, dv)`` float64 rasters for the loss
+    ``sum(dout * out)``.  ``q, k, v, dout``: float32 rasters
+    ``[B, T, H, W, heads, d]`` holding the exact input values."""
+    q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+    B, T, H, W, heads, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and dout.shape == q.shape and (T, H, W) == tuple(dims)
+    if scale is None:
+        scale = default_scale(d)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    dq, dk, dv = (np.empty(q.shape, dtype=np.float64) for _ in range(3))
+    arr3 = ctypes.c_int * 3
+    rc = _load().gna_oracle_backward(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, B, heads,
+        arr3(*dims), arr3(*window), arr3(*stride), d, _rule_code(rule), float(scale),
+        dq.ctypes.data, dk.ctypes.data, dv.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError(f"gna_oracle_backward failed with {rc}")
+    return dq, dk, dv

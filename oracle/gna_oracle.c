@@ -172,3 +172,141 @@ int gna_oracle_forward(const float *q, const float *k, const float *v,
     free(th);
     return rc;
 }
+
+/*
+ * Backward pass: the derivative of the forward above (the GNA page asks for
+ * training with GNA, §4.2 problem 1 and §5, and writes no backward; this is
+ * the chain rule applied to the definition).  For L = sum_i <dout_i, out_i>:
+ *
+ *   p_ij   = exp(s_ij - lse_i)                for j in N(i)
+ *   dv_j  += p_ij dout_i
+ *   dp_ij  = <dout_i, v_j>
+ *   ds_ij  = p_ij (dp_ij - sum_l p_il dp_il)
+ *   dq_i   = scale sum_j ds_ij k_j
+ *   dk_j  += scale ds_ij q_i
+ *
+ * A thread owns whole (b, head) planes, so the scatters into dk and dv of one
+ * plane never race.
+ */
+typedef struct {
+    const float *q, *k, *v, *dout;
+    int B, heads, dims[3], win[3], str[3], d, rule;
+    double scale;
+    int p_begin, p_end;
+    double *dq, *dk, *dv;
+    int status;
+} bjob_t;
+
+static int64_t row_of(const bjob_t *J, int b, int t, int y, int x, int h)
+{
+    return ((((int64_t)b * J->dims[0] + t) * J->dims[1] + y) * J->dims[2] + x) * J->heads + h;
+}
+
+static void backward_plane(const bjob_t *J, int plane, double *pbuf, double *dpbuf)
+{
+    const int T = J->dims[0], H = J->dims[1], W = J->dims[2], d = J->d;
+    const int b = plane / J->heads, h = plane % J->heads;
+    for (int t = 0; t < T; ++t)
+        for (int y = 0; y < H; ++y)
+            for (int x = 0; x < W; ++x) {
+                const int a0 = start_of(t, T, J->win[0], J->str[0], J->rule);
+                const int a1 = start_of(y, H, J->win[1], J->str[1], J->rule);
+                const int a2 = start_of(x, W, J->win[2], J->str[2], J->rule);
+                const int64_t qi = row_of(J, b, t, y, x, h) * d;
+                /* probabilities of the window (max subtracted), and dp */
+                int64_t n = 0;
+                double m = -INFINITY;
+                for (int kt = a0; kt < a0 + J->win[0]; ++kt)
+                    for (int ky = a1; ky < a1 + J->win[1]; ++ky)
+                        for (int kx = a2; kx < a2 + J->win[2]; ++kx) {
+                            const int64_t kj = row_of(J, b, kt, ky, kx, h) * d;
+                            double acc = 0.0, dacc = 0.0;
+                            for (int c = 0; c < d; ++c) {
+                                acc += (double)J->q[qi + c] * (double)J->k[kj + c];
+                                dacc += (double)J->dout[qi + c] * (double)J->v[kj + c];
+                            }
+                            pbuf[n] = J->scale * acc;
+                            dpbuf[n] = dacc;
+                            if (pbuf[n] > m) m = pbuf[n];
+                            ++n;
+                        }
+                double z = 0.0;
+                for (int64_t l = 0; l < n; ++l) { pbuf[l] = exp(pbuf[l] - m); z += pbuf[l]; }
+                double dsum = 0.0;
+                for (int64_t l = 0; l < n; ++l) { pbuf[l] /= z; dsum += pbuf[l] * dpbuf[l]; }
+                /* scatter */
+                n = 0;
+                for (int kt = a0; kt < a0 + J->win[0]; ++kt)
+                    for (int ky = a1; ky < a1 + J->win[1]; ++ky)
+                        for (int kx = a2; kx < a2 + J->win[2]; ++kx) {
+                            const int64_t kj = row_of(J, b, kt, ky, kx, h) * d;
+                            const double p = pbuf[n];
+                            const double ds = p * (dpbuf[n] - dsum);
+                            ++n;
+                            for (int c = 0; c < d; ++c) {
+                                J->dq[qi + c] += J->scale * ds * (double)J->k[kj + c];
+                                J->dk[kj + c] += J->scale * ds * (double)J->q[qi + c];
+                                J->dv[kj + c] += p * (double)J->dout[qi + c];
+                            }
+                        }
+            }
+}
+
+static void *bworker(void *arg)
+{
+    bjob_t *J = (bjob_t *)arg;
+    int64_t wsz = (int64_t)J->win[0] * J->win[1] * J->win[2];
+    double *pbuf = (double *)malloc(sizeof(double) * (size_t)wsz);
+    double *dpbuf = (double *)malloc(sizeof(double) * (size_t)wsz);
+    if (!pbuf || !dpbuf) { free(pbuf); free(dpbuf); J->status = -2; return NULL; }
+    for (int plane = J->p_begin; plane < J->p_end; ++plane) backward_plane(J, plane, pbuf, dpbuf);
+    free(pbuf);
+    free(dpbuf);
+    return NULL;
+}
+
+/*
+ * q, k, v, dout : float32 rasters [B, T, H, W, heads, d] (exact input values)
+ * dq, dk, dv    : double rasters of the same shape, overwritten
+ * Returns 0, -1 on invalid arguments, -2 on allocation failure.
+ */
+int gna_oracle_backward(const float *q, const float *k, const float *v, const float *dout,
+                        int B, int heads, const int dims[3], const int window[3],
+                        const int stride[3], int head_dim, int rule, double scale,
+                        double *dq, double *dk, double *dv, int nthreads)
+{
+    if (B < 1 || heads < 1 || head_dim < 1 || (rule != 0 && rule != 1)) return -1;
+    for (int i = 0; i < 3; ++i)
+        if (!(1 <= stride[i] && stride[i] <= window[i] && window[i] <= dims[i])) return -1;
+    const int64_t n_el = (int64_t)B * dims[0] * dims[1] * dims[2] * heads * head_dim;
+    memset(dq, 0, sizeof(double) * (size_t)n_el);
+    memset(dk, 0, sizeof(double) * (size_t)n_el);
+    memset(dv, 0, sizeof(double) * (size_t)n_el);
+    const int planes = B * heads;
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > planes) nthreads = planes;
+    bjob_t *jobs = (bjob_t *)calloc((size_t)nthreads, sizeof(bjob_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return -2; }
+    for (int i = 0; i < nthreads; ++i) {
+        bjob_t *J = &jobs[i];
+        J->q = q; J->k = k; J->v = v; J->dout = dout;
+        J->B = B; J->heads = heads; J->d = head_dim; J->rule = rule; J->scale = scale;
+        for (int c = 0; c < 3; ++c) { J->dims[c] = dims[c]; J->win[c] = window[c]; J->str[c] = stride[c]; }
+        J->dq = dq; J->dk = dk; J->dv = dv;
+        J->p_begin = (int)((int64_t)planes * i / nthreads);
+        J->p_end = (int)((int64_t)planes * (i + 1) / nthreads);
+        J->status = 0;
+    }
+    int rc = 0;
+    if (nthreads == 1) {
+        bworker(&jobs[0]);
+    } else {
+        for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, bworker, &jobs[i]);
+        for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    }
+    for (int i = 0; i < nthreads; ++i) if (jobs[i].status) rc = jobs[i].status;
+    free(jobs);
+    free(th);
+    return rc;
+}

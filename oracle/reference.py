@@ -122,6 +122,67 @@ def gna_forward_loops(q, k, v, dims, window, stride, scale=None, rule=LEADER_CEN
     return out, lse
 
 
+def softmax_backward(p: np.ndarray, dp: np.ndarray) -> np.ndarray:
+    """Gradient of the scores from the gradient of the probabilities.
+
+    For p = softmax(s), the Jacobian dp_j/ds_l = p_j (delta_jl - p_l), so
+    ds_l = p_l (dp_l - sum_j p_j dp_j).
+    """
+    return p * (dp - (p * dp).sum())
+
+
+def gna_backward_loops(q, k, v, dout, dims, window, stride, scale=None, rule=LEADER_CENTER):
+    """Gradients of the GNA forward, one query at a time (float64).
+
+    The GNA page asks for training with GNA in the loop (§4.2, problem 1: add
+    GNA during training, not only at inference; §5: fold GNA into training) but
+    writes no backward pass.  The reading taken here: the backward is the
+    derivative of the forward definition above.  For the loss
+    ``L = sum_i <dout_i, out_i>`` it returns ``dL/dq, dL/dk, dL/dv``, arrays
+    ``[B, T, H, W, heads, d]``.  With p_ij = exp(s_ij - lse_i) for j in N(i):
+
+        dv_j  += p_ij dout_i                        (out_i is linear in v_j)
+        dp_ij  = <dout_i, v_j>
+        ds_ij  = p_ij (dp_ij - sum_l p_il dp_il)    (softmax Jacobian)
+        dq_i   = scale sum_j ds_ij k_j
+        dk_j  += scale ds_ij q_i
+
+    A key collects from every query whose window holds it.  Pure-Python loop
+    over queries: small grids only.
+    """
+    check_geometry(dims, window, stride)
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    B, T, H, W, heads, d = q.shape
+    assert (T, H, W) == tuple(dims) and k.shape == q.shape and v.shape == q.shape and dout.shape == q.shape
+    if scale is None:
+        scale = default_scale(d)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for idx in itertools.product(range(T), range(H), range(W)):
+            keys = neighborhood(idx, dims, window, stride, rule)
+            kt, ky, kx = (np.array(c) for c in zip(*keys))
+            for h in range(heads):
+                qi = q[(b,) + idx + (h,)]
+                doi = dout[(b,) + idx + (h,)]
+                kk = k[b, kt, ky, kx, h]          # [|N|, d]
+                vv = v[b, kt, ky, kx, h]
+                s = scale * (kk @ qi)
+                e = np.exp(s - s.max())
+                p = e / e.sum()
+                dp = vv @ doi
+                ds = softmax_backward(p, dp)
+                dq[(b,) + idx + (h,)] = scale * (ds @ kk)
+                # keys of one window are distinct, so these scatters never collide
+                dk[b, kt, ky, kx, h] += scale * ds[:, None] * qi[None, :]
+                dv[b, kt, ky, kx, h] += p[:, None] * doi[None, :]
+    return dq, dk, dv
+
+
 def window_mask(dims, window, stride, rule=LEADER_CENTER) -> np.ndarray:
     """Boolean ``[N, N]`` matrix, ``mask[i, j]`` true iff key j is in the window of query i.
 
