@@ -522,10 +522,104 @@ gna_status gna_forward_raster(const void* q, const void* k, const void* v, void*
 
 gna_status gna_get_status(void* stream)
 {
-    int status = 0;
+    int status = 0, bwd_status = 0;
     cudaError_t e = gna::read_and_clear_status(&status, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "status read");
+    e = gna::read_and_clear_bwd_status(&bwd_status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (status == 0) status = bwd_status;
     if (status != 0) return fail(static_cast<gna_status>(status), "a kernel abandoned a pipeline wait");
+    return GNA_OK;
+}
+
+namespace {
+
+// Shared checks of the backward entry points: geometry, dtype, head_dim,
+// options; fills the tile and the tiled row count.
+gna_status backward_common(int B, int heads, const int dims[3], const int window[3], const int stride[3],
+                           int head_dim, gna_dtype dtype, const gna_options* opt, int tile[3], int tlog[3],
+                           int64_t* num_q_tiles)
+{
+    if (B < 1 || heads < 1) return fail(GNA_ERR_INVALID_ARG, "B and heads must be >= 1");
+    gna_status st = check_geometry(dims, window, stride);
+    if (st != GNA_OK) return st;
+    if (dtype != GNA_BF16 || head_dim != 128)
+        return fail(GNA_ERR_UNSUPPORTED, "the backward pass supports bf16 with head_dim 128");
+    const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
+    if (rule != GNA_LEADER_CENTER && rule != GNA_LEADER_LITERAL)
+        return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", rule);
+    if (opt && !(opt->scale >= 0.0f && std::isfinite(opt->scale)))
+        return fail(GNA_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    if (opt && opt->descale) return fail(GNA_ERR_INVALID_ARG, "descale is only used with GNA_FP8_E4M3");
+    st = resolve_tile(dims, opt ? opt->tile : nullptr, tile, tlog);
+    if (st != GNA_OK) return st;
+    int64_t n = static_cast<int64_t>(B) * heads;
+    for (int d = 0; d < 3; ++d) n *= (dims[d] + tile[d] - 1) / tile[d];
+    if (n * gna::kTileElems > INT32_MAX) return fail(GNA_ERR_UNSUPPORTED, "more than 2^31 tiled rows");
+    *num_q_tiles = n;
+    return GNA_OK;
+}
+
+}  // namespace
+
+gna_status gna_backward_delta(const void* out, const void* dout, float* delta, int B, int heads, const int dims[3],
+                              int head_dim, gna_dtype dtype, const gna_options* opt, void* stream)
+{
+    if (out == nullptr || dout == nullptr || delta == nullptr) return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(out) || !aligned16(dout) || !aligned16(delta))
+        return fail(GNA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    if (!dims_ok(dims)) return fail(GNA_ERR_INVALID_ARG, "dims must be >= 1");
+    int tile[3], tlog[3];
+    int64_t nq = 0;
+    gna_status st = backward_common(B, heads, dims, dims, dims, head_dim, dtype, opt, tile, tlog, &nq);
+    if (st != GNA_OK) return st;
+    cudaError_t e = gna::launch_backward_delta(out, dout, delta, nq * gna::kTileElems, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward delta launch");
+    t_last_error.clear();
+    return GNA_OK;
+}
+
+gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, const void* v, const void* dout,
+                           const float* lse, const float* delta, void* dq, int B, int heads, const int dims[3],
+                           const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
+                           const gna_options* opt, void* stream)
+{
+    if (!q || !k || !k_value || !v || !dout || !lse || !delta || !dq)
+        return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(k_value) || !aligned16(v) || !aligned16(dout) ||
+        !aligned16(lse) || !aligned16(delta) || !aligned16(dq))
+        return fail(GNA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    int tile[3], tlog[3];
+    int64_t nq = 0;
+    gna_status st = backward_common(B, heads, dims, window, stride, head_dim, dtype, opt, tile, tlog, &nq);
+    if (st != GNA_OK) return st;
+    const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
+    gna::BwdParams p{};
+    int64_t tiles_per_head = 1;
+    for (int d = 0; d < 3; ++d) {
+        p.dims[d] = dims[d];
+        p.win[d] = window[d];
+        p.str[d] = stride[d];
+        p.off[d] = gna::leader_offset(stride[d], rule);
+        p.tile[d] = tile[d];
+        p.tlog[d] = tlog[d];
+        p.nt[d] = (dims[d] + tile[d] - 1) / tile[d];
+        tiles_per_head *= p.nt[d];
+    }
+    p.tiles_per_head = static_cast<int>(tiles_per_head);
+    p.scale = (opt && opt->scale > 0.0f) ? opt->scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    p.q = q;
+    p.dout = dout;
+    p.lse = lse;
+    p.delta = delta;
+    p.dq = dq;
+    const int64_t rows = nq * gna::kTileElems;
+    if ((st = make_tile_map(&p.tmK, k, rows, head_dim, 2)) != GNA_OK) return st;
+    if ((st = make_tile_map(&p.tmV, v, rows, head_dim, 2)) != GNA_OK) return st;
+    if ((st = make_value_map(&p.tmKv, k_value, nq, head_dim, 2)) != GNA_OK) return st;
+    cudaError_t e = gna::launch_backward_dq(p, nq, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward dq launch");
+    t_last_error.clear();
     return GNA_OK;
 }
 

@@ -54,4 +54,28 @@ cudaError_t launch_forward(const FwdParams& p, int head_dim, int elem_size, int6
 // Device status word: read-and-clear.
 cudaError_t read_and_clear_status(int* status, cudaStream_t stream);
 
+// Parameters of one dQ launch of the backward pass (bf16, head_dim 128; all
+// tensors tiled except kv, which is k in the value layout).
+struct BwdParams {
+    CUtensorMap tmK;             // 2-D TMA view [rows, 128] of the tiled k
+    CUtensorMap tmV;             // 2-D TMA view [rows, 128] of the tiled v
+    CUtensorMap tmKv;            // 2-D TMA view [rows, 128] of k in the value layout
+    const void* q;               // tiled q [rows, 128]
+    const void* dout;            // tiled dout [rows, 128]
+    const float* lse;            // tiled lse [rows] of the forward (natural log)
+    const float* delta;          // tiled <dout, out> [rows]
+    void* dq;                    // tiled bf16 dq [rows, 128]
+    int dims[3], win[3], str[3], off[3];
+    int tile[3], tlog[3], nt[3];
+    int tiles_per_head;
+    float scale;
+};
+
+// dQ over num_q_tiles CTAs, and delta = <dout, out> over `rows` tiled rows.
+cudaError_t launch_backward_dq(const BwdParams& p, int64_t num_q_tiles, cudaStream_t stream);
+cudaError_t launch_backward_delta(const void* out, const void* dout, float* delta, int64_t rows,
+                                  cudaStream_t stream);
+// Status word of the backward kernels: read-and-clear.
+cudaError_t read_and_clear_bwd_status(int* status, cudaStream_t stream);
+
 }  // namespace gna

@@ -93,6 +93,11 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(GNAOptions), _P]
         L.gna_forward_raster.restype = st
         L.gna_forward_raster.argtypes = L.gna_forward_ex.argtypes
+        L.gna_backward_delta.restype = st
+        L.gna_backward_delta.argtypes = [_P, _P, _P, _INT, _INT, _I3, _INT, _INT, ctypes.POINTER(GNAOptions), _P]
+        L.gna_backward_dq.restype = st
+        L.gna_backward_dq.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _INT,
+                                      ctypes.POINTER(GNAOptions), _P]
         L.gna_tile_stats.restype = st
         L.gna_tile_stats.argtypes = [_I3, _I3, _I3, _P, _INT, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
@@ -317,6 +322,43 @@ def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: t
     _check(lib().gna_forward_raster(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                     _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
                                     _stream_ptr(stream)))
+
+
+def gna_backward_delta(out: torch.Tensor, dout: torch.Tensor, delta: torch.Tensor, B: int, heads: int, dims,
+                       head_dim: int, *, tile=None, stream=None):
+    """delta = <dout, out> per tiled row (see ``include/gna.h``); bf16 in, float32 out."""
+    if out.dtype != torch.bfloat16 or dout.dtype != torch.bfloat16 or delta.dtype != torch.float32:
+        raise ValueError("out, dout must be bfloat16 and delta float32")
+    nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
+    _need(out=(out, nt), dout=(dout, nt), delta=(delta, nt // head_dim))
+    opt = GNAOptions()
+    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+    _check(lib().gna_backward_delta(_ptr(out), _ptr(dout), _ptr(delta), B, heads, _I3(*dims), head_dim, GNA_BF16,
+                                    ctypes.byref(opt), _stream_ptr(stream)))
+
+
+def gna_backward_dq(q: torch.Tensor, k: torch.Tensor, k_value: torch.Tensor, v: torch.Tensor, dout: torch.Tensor,
+                    lse: torch.Tensor, delta: torch.Tensor, dq: torch.Tensor, B: int, heads: int, dims, window,
+                    stride, head_dim: int, *, tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0,
+                    stream=None):
+    """dq of the GNA forward (see ``include/gna.h``): tiled bf16 tensors, ``k_value``
+    in the value layout, the forward's tiled ``lse`` and ``delta`` from
+    :func:`gna_backward_delta`."""
+    for name, t in (("q", q), ("k", k), ("k_value", k_value), ("v", v), ("dout", dout), ("dq", dq)):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+    if lse.dtype != torch.float32 or delta.dtype != torch.float32:
+        raise ValueError("lse and delta must be float32")
+    nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
+    _need(q=(q, nt), k=(k, nt), k_value=(k_value, nt), v=(v, nt), dout=(dout, nt), dq=(dq, nt),
+          lse=(lse, nt // head_dim), delta=(delta, nt // head_dim))
+    opt = GNAOptions()
+    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+    opt.leader_rule = leader_rule
+    opt.scale = scale
+    _check(lib().gna_backward_dq(_ptr(q), _ptr(k), _ptr(k_value), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta),
+                                 _ptr(dq), B, heads, _I3(*dims), _I3(*window), _I3(*stride), head_dim, GNA_BF16,
+                                 ctypes.byref(opt), _stream_ptr(stream)))
 
 
 def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADER_CENTER):

@@ -185,6 +185,38 @@ gna_status gna_forward_raster(const void* q, const void* k, const void* v, void*
                               int B, int heads, const int dims[3], const int window[3], const int stride[3],
                               int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
 
+/* ------------------------------------------------------------ backward ---- */
+
+/* The GNA page asks for GNA in training (§4.2, problem 1; §5) and writes no
+ * backward; the backward here is the derivative of the forward for the loss
+ * L = sum_i <dout_i, out_i>.  It runs in two calls, both bf16 with head_dim
+ * 128, all tensors in the tiled layout of the forward (same tile):
+ *
+ * gna_backward_delta: delta_i = <dout_i, out_i> (fp32), the row term of the
+ * softmax Jacobian, from the forward's bf16 out.
+ *   out, dout : tiled [B, heads, tiles, 128, 128] bfloat16
+ *   delta     : tiled [B, heads, tiles, 128] float32, written (caller-owned
+ *               workspace of the dq call)
+ *   opt       : tile (NULL or zero = default); other fields must be defaults
+ *
+ * gna_backward_dq: dq_i = scale sum_{j in N(i)} p_ij (<dout_i, v_j> - delta_i) k_j
+ * with p_ij = exp(scale <q_i, k_j> - lse_i).
+ *   q, k, v, dout : tiled bfloat16 (the forward's inputs and the gradient of out)
+ *   k_value       : k in the value layout (gna_permute_v, same tile)
+ *   lse           : the forward's tiled lse; delta: from gna_backward_delta
+ *   dq            : tiled bfloat16, written (padding rows zero)
+ *   window, stride, opt : as given to the forward
+ * Asynchronous on `stream`; a kernel that abandons a wait reports through
+ * gna_get_status.  GNA_ERR_UNSUPPORTED for other dtypes or head_dims,
+ * GNA_ERR_INVALID_ARG as gna_forward_ex.  dk and dv are not computed yet. */
+gna_status gna_backward_delta(const void* out, const void* dout, float* delta, int B, int heads,
+                              const int dims[3], int head_dim, gna_dtype dtype, const gna_options* opt,
+                              void* stream);
+gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, const void* v,
+                           const void* dout, const float* lse, const float* delta, void* dq, int B,
+                           int heads, const int dims[3], const int window[3], const int stride[3],
+                           int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
+
 /* ------------------------------------------------------------ planning ---- */
 
 /* Tile statistics of one (b, head) plane under the given tile (NULL =

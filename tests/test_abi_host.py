@@ -251,3 +251,17 @@ def test_binding_checks_tensor_sizes_before_any_call():
     # sizes right: the next refusal is the device check (CPU tensors)
     with pytest.raises(ValueError, match="CUDA device"):
         G.gna_forward(ok_tiled, ok_tiled, ok_tiled, ok_tiled, None, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
+
+
+def test_backward_rejects_bad_arguments_on_host(L):
+    dims, win, st = I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1)
+    args = (FAKE,) * 8
+    assert L.gna_backward_dq(None, *args[1:], 1, 2, dims, win, st, 128, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_INVALID_ARG
+    assert L.gna_backward_dq(*args, 1, 2, dims, win, st, 64, G.GNA_BF16, None, None) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_backward_dq(*args, 1, 2, dims, win, st, 128, G.GNA_FP8_E4M3, None, None) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_backward_dq(*args, 1, 2, dims, I3(1, 17, 5), st, 128, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_INVALID_ARG
+    assert L.gna_backward_delta(FAKE, FAKE + 8, FAKE, 1, 2, dims, 128, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_INVALID_ARG
+    assert L.gna_backward_delta(FAKE, FAKE, FAKE, 0, 2, dims, 128, G.GNA_BF16, None, None) == G.GNA_ERR_INVALID_ARG

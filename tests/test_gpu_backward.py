@@ -1,0 +1,88 @@
+"""dQ of the CUDA backward (``gna_backward_delta`` + ``gna_backward_dq``) against
+the pinned backward oracle, every element compared.
+
+The GPU path reads the bf16 out and lse of its own forward; the oracle
+recomputes everything in float64 from the same bf16 inputs.  The differences
+come from bf16 dS, bf16 out in delta and the bf16 result, so the bar is a
+relative one: relative RMS < 2e-2 and max |error| <= 5 % of max |dq|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from dimensional_sparse_attention_gna_b300 import gna as G
+from synthetic_inputs import exact_f32, normal_raster, to_bf16
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_dq(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
+    B, T, H, W, heads, d = q.shape
+    dev = torch.device("cuda")
+    shp = G.tiled_shape(B, heads, dims, d, tile)
+    tiled = {}
+    for name, x in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
+        G.gna_permute(x.to(dev).contiguous(), t, B, heads, dims, d, tile=tile)
+        tiled[name] = t
+    vshape = G.value_shape(B, heads, dims, d, tile)
+    k_val, v_val = (torch.empty(vshape, dtype=torch.bfloat16, device=dev) for _ in range(2))
+    G.gna_permute_v(k.to(dev).contiguous(), k_val, B, heads, dims, d, tile=tile)
+    G.gna_permute_v(v.to(dev).contiguous(), v_val, B, heads, dims, d, tile=tile)
+    out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
+    lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
+    G.gna_forward(tiled["q"], tiled["k"], v_val, out_t, lse_t, B, heads, dims, window, stride, d, tile=tile,
+                  leader_rule=rule)
+    delta = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
+    G.gna_backward_delta(out_t, tiled["dout"], delta, B, heads, dims, d, tile=tile)
+    dq_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
+    G.gna_backward_dq(tiled["q"], tiled["k"], k_val, tiled["v"], tiled["dout"], lse_t, delta, dq_t, B, heads, dims,
+                      window, stride, d, tile=tile, leader_rule=rule)
+    dq = torch.empty((B,) + tuple(dims) + (heads, d), dtype=torch.bfloat16, device=dev)
+    G.gna_unpermute(dq_t, dq, B, heads, dims, d, tile=tile)
+    G.gna_get_status()
+    torch.cuda.synchronize()
+    return dq.float().cpu().numpy(), dq_t
+
+
+def _check_dq(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
+    d = 128
+    q, k, v, dout = (to_bf16(normal_raster(seed + i, B, dims, heads, d)) for i in range(4))
+    dq, _ = gpu_dq(q, k, v, dout, dims, window, stride, tile=tile, rule=rule)
+    orule = oracle.LEADER_CENTER if rule == G.GNA_LEADER_CENTER else oracle.LEADER_LITERAL
+    dq_ref, _, _ = oracle.backward_c(exact_f32(q), exact_f32(k), exact_f32(v), exact_f32(dout), dims, window,
+                                     stride, rule=orule)
+    err = np.abs(dq.astype(np.float64) - dq_ref)
+    rel = float(np.sqrt((err ** 2).mean() / (dq_ref ** 2).mean()))
+    info = f"max|err|={err.max():.3e} max|dq|={np.abs(dq_ref).max():.3e} relRMS={rel:.3e}"
+    assert np.isfinite(dq).all(), info
+    assert rel < 2e-2, info
+    assert err.max() <= 0.05 * np.abs(dq_ref).max(), info
+    return rel
+
+
+@pytest.mark.parametrize("B,heads,dims,window,stride,tile,rule", [
+    (1, 2, (4, 16, 20), (3, 7, 9), (1, 1, 1), None, G.GNA_LEADER_CENTER),
+    (2, 2, (5, 19, 23), (3, 9, 11), (1, 2, 3), None, G.GNA_LEADER_CENTER),     # ragged: every tile padded
+    (1, 2, (6, 20, 24), (4, 8, 8), (2, 4, 4), None, G.GNA_LEADER_LITERAL),
+    (1, 2, (3, 17, 40), (3, 7, 13), (1, 2, 5), (1, 8, 16), G.GNA_LEADER_CENTER),
+    (1, 3, (1, 45, 37), (1, 12, 9), (1, 1, 1), None, G.GNA_LEADER_CENTER),     # 2-D
+    (1, 2, (2, 8, 16), (2, 8, 16), (1, 1, 1), None, G.GNA_LEADER_CENTER),      # window = grid
+    (1, 2, (4, 16, 16), (2, 8, 8), (2, 8, 8), None, G.GNA_LEADER_CENTER),      # blocked
+])
+def test_dq_small_grids_all_elements(B, heads, dims, window, stride, tile, rule):
+    _check_dq(8000 + sum(dims), B, heads, dims, window, stride, tile=tile, rule=rule)
+
+
+def test_dq_mid_size_video_grid():
+    """Several KV tiles per dimension and full interior tiles (8x24x40 tokens, 4 heads)."""
+    _check_dq(8100, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1))
+
+
+def test_dq_repeat_runs_bit_identical():
+    dims, window, stride, d = (4, 16, 24), (3, 9, 11), (1, 2, 3), 128
+    q, k, v, dout = (to_bf16(normal_raster(8200 + i, 1, dims, 2, d)) for i in range(4))
+    _, a = gpu_dq(q, k, v, dout, dims, window, stride)
+    _, b = gpu_dq(q, k, v, dout, dims, window, stride)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
