@@ -579,6 +579,49 @@ gna_status gna_backward_delta(const void* out, const void* dout, float* delta, i
     return GNA_OK;
 }
 
+gna_status gna_backward_dkdv(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                             const float* delta, void* dk, void* dv, int B, int heads, const int dims[3],
+                             const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
+                             const gna_options* opt, void* stream)
+{
+    if (!q || !k || !v || !dout || !lse || !delta || !dk || !dv) return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(lse) || !aligned16(delta) ||
+        !aligned16(dk) || !aligned16(dv))
+        return fail(GNA_ERR_INVALID_ARG, "pointers must be 16-byte aligned");
+    int tile[3], tlog[3];
+    int64_t nt_all = 0;
+    gna_status st = backward_common(B, heads, dims, window, stride, head_dim, dtype, opt, tile, tlog, &nt_all);
+    if (st != GNA_OK) return st;
+    const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
+    gna::BwdKVParams p{};
+    int64_t tiles_per_head = 1;
+    for (int d = 0; d < 3; ++d) {
+        p.dims[d] = dims[d];
+        p.win[d] = window[d];
+        p.str[d] = stride[d];
+        p.off[d] = gna::leader_offset(stride[d], rule);
+        p.tile[d] = tile[d];
+        p.tlog[d] = tlog[d];
+        p.nt[d] = (dims[d] + tile[d] - 1) / tile[d];
+        tiles_per_head *= p.nt[d];
+    }
+    p.tiles_per_head = static_cast<int>(tiles_per_head);
+    p.scale = (opt && opt->scale > 0.0f) ? opt->scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
+    p.lse = lse;
+    p.delta = delta;
+    p.dk = dk;
+    p.dv = dv;
+    const int64_t rows = nt_all * gna::kTileElems;
+    if ((st = make_tile_map(&p.tmQ, q, rows, head_dim, 2)) != GNA_OK) return st;
+    if ((st = make_tile_map(&p.tmDO, dout, rows, head_dim, 2)) != GNA_OK) return st;
+    if ((st = make_tile_map(&p.tmK, k, rows, head_dim, 2)) != GNA_OK) return st;
+    if ((st = make_tile_map(&p.tmV, v, rows, head_dim, 2)) != GNA_OK) return st;
+    cudaError_t e = gna::launch_backward_dkdv(p, nt_all, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "backward dk/dv launch");
+    t_last_error.clear();
+    return GNA_OK;
+}
+
 gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, const void* v, const void* dout,
                            const float* lse, const float* delta, void* dq, int B, int heads, const int dims[3],
                            const int window[3], const int stride[3], int head_dim, gna_dtype dtype,

@@ -400,6 +400,366 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
     }
 }
 
+// ---------------------------------------------------------------------------- dK, dV
+//
+// One CTA per 128-key tile j of one (batch, head).  It visits the Q tiles
+// whose windows reach tile j: per dimension the KV box [k0(qt), k1(qt)] of a Q
+// tile moves monotonically with qt, so those Q tiles form an interval per
+// dimension (the inverse box).  Per Q tile i:
+//   S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T            (A, B from shared memory)
+//   P^T  = exp(S^T - lse_i),  dS^T = P^T (dP^T - delta_i)   (per key row)
+//   dV_j += P^T dO_i,  dK_j += dS^T Q_i               (A from TMEM, B MN-major)
+// TMEM: dV [0, 128), dK [128, 256), S^T [256, 384), dP^T [384, 512); each
+// thread half writes its P^T / dS^T columns over the front of its own S^T /
+// dP^T columns.  Q_i and dO_i are read as tiled tiles in both roles: K-major
+// for S^T and dP^T, MN-major (token rows, 16 per k-step) for dV and dK.
+// The element mask comes from, per dimension, the interval of query
+// positions whose window holds this thread's key; a key row whose interval
+// covers the whole Q tile needs no mask.
+
+constexpr uint32_t kColDV = 0;
+constexpr uint32_t kColDK = 128;
+constexpr uint32_t kColST = 256;
+constexpr uint32_t kColDPT = 384;
+constexpr int kKVStageBytes = 2 * kTileBytes + 1024;            // Q_i, dO_i, lse_i, delta_i (1024-aligned)
+constexpr int kKVSmemAlloc = 2 * kTileBytes + kBStages * kKVStageBytes + 1024;
+constexpr uint32_t kIdescMN = make_idesc(128, 128, kFmtBF16, true);
+
+struct KVBars {
+    uint64_t kv_full;             // K_j and V_j landed
+    uint64_t full[kBStages];      // Q_i, dO_i, lse_i, delta_i landed
+    uint64_t empty[kBStages];     // the four MMAs of step i are done
+    uint64_t sdp_full;            // S^T and dP^T of step i are in TMEM
+    uint64_t p_full;              // P^T and dS^T of step i are in TMEM (8 warps)
+    uint64_t final_;              // the last dV / dK products are done
+    uint64_t drain;
+};
+
+__global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid_constant__ BwdKVParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ KVBars bars;
+    __shared__ uint32_t tmem_base_sh;
+    __shared__ volatile int abort_flag;
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+
+    // ---------------------------------------------------------------- geometry
+    const int64_t kv_tile_global = blockIdx.x;                // (b*heads + h)*tiles_per_head + kt
+    const int kt_id = static_cast<int>(kv_tile_global % p.tiles_per_head);
+    const int64_t plane_base = kv_tile_global - kt_id;        // first tile of this (b, head) plane
+    int kc[3];
+    kc[2] = kt_id % p.nt[2];
+    kc[1] = (kt_id / p.nt[2]) % p.nt[1];
+    kc[0] = kt_id / (p.nt[2] * p.nt[1]);
+    BwdBox qbox;                                              // inverse box: Q tiles reaching tile kc
+#pragma unroll
+    for (int d = 0; d < 3; ++d) {
+        int lo = -1, hi = -2;
+        for (int qt = 0; qt < p.nt[d]; ++qt) {
+            const DimRange r = dim_range(qt, p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
+            if (r.k0 <= kc[d] && kc[d] <= r.k1) {
+                if (lo < 0) lo = qt;
+                hi = qt;
+            }
+        }
+        qbox.k0[d] = lo < 0 ? 0 : lo;
+        qbox.cnt[d] = lo < 0 ? 0 : hi - lo + 1;
+    }
+    const int n_q = qbox.cnt[0] * qbox.cnt[1] * qbox.cnt[2];
+
+    auto bar = [](uint64_t& b) { return smem_u32(&b); };
+    const uint32_t sK = smem_u32(smem);
+    const uint32_t sV = sK + kTileBytes;
+    const uint32_t sStage = sK + 2 * kTileBytes;
+    const float* stage_f = reinterpret_cast<const float*>(smem + 2 * kTileBytes);   // float view of the stages
+
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(bar(bars.kv_full), 1);
+        for (int s = 0; s < kBStages; ++s) {
+            mbar_init(bar(bars.full[s]), 1);
+            mbar_init(bar(bars.empty[s]), 1);
+        }
+        mbar_init(bar(bars.sdp_full), 1);
+        mbar_init(bar(bars.p_full), kBSoftmaxWarps);
+        mbar_init(bar(bars.final_), 1);
+        mbar_init(bar(bars.drain), 1);
+        fence_mbarrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_base_sh), kBTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_sh;
+
+    if (warp == 0) {
+        // ============================================================ TMA producer
+        if (elect_one_sync()) {
+            prefetch_tensormap(&p.tmQ);
+            prefetch_tensormap(&p.tmDO);
+            prefetch_tensormap(&p.tmK);
+            prefetch_tensormap(&p.tmV);
+        }
+        if (n_q > 0 && elect_one_sync()) {
+            const int32_t row = static_cast<int32_t>(kv_tile_global * kTileElems);
+            mbar_arrive_expect_tx(bar(bars.kv_full), 2 * kTileBytes);
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                tma_load_2d(sK + c * kTileElems * 128, &p.tmK, bar(bars.kv_full), c * 64, row);
+                tma_load_2d(sV + c * kTileElems * 128, &p.tmV, bar(bars.kv_full), c * 64, row);
+            }
+        }
+        __syncwarp();
+        int issued = 0;
+        bool early = false;
+        int qc[3] = {qbox.k0[0], qbox.k0[1], qbox.k0[2]};
+        for (int i = 0; i < n_q; ++i, bwd_odometer(qc, qbox)) {
+            const int s = i % kBStages;
+            const int64_t qtile = plane_base + (qc[0] * p.nt[1] + qc[1]) * p.nt[2] + qc[2];
+            if (i >= kBStages &&
+                !__all_sync(0xffffffffu, mbar_wait(bar(bars.empty[s]), ((i / kBStages) & 1) ^ 1, &abort_flag))) {
+                early = true;
+                break;
+            }
+            if (elect_one_sync()) {
+                const uint32_t st = sStage + s * kKVStageBytes;
+                const int32_t row = static_cast<int32_t>(qtile * kTileElems);
+                mbar_arrive_expect_tx(bar(bars.full[s]), 2 * kTileBytes + 2 * kTileElems * 4);
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    tma_load_2d(st + c * kTileElems * 128, &p.tmQ, bar(bars.full[s]), c * 64, row);
+                    tma_load_2d(st + kTileBytes + c * kTileElems * 128, &p.tmDO, bar(bars.full[s]), c * 64, row);
+                }
+                bulk_load_g2s(st + 2 * kTileBytes, p.lse + qtile * kTileElems, kTileElems * 4, bar(bars.full[s]));
+                bulk_load_g2s(st + 2 * kTileBytes + kTileElems * 4, p.delta + qtile * kTileElems, kTileElems * 4,
+                              bar(bars.full[s]));
+            }
+            __syncwarp();
+            ++issued;
+        }
+        if (early) {
+            if (lane == 0) bwd_raise(&abort_flag);
+            const volatile int never = 0;
+            for (int i = (issued > kBStages ? issued - kBStages : 0); i < issued; ++i)
+                mbar_wait(bar(bars.full[i % kBStages]), (i / kBStages) & 1, &never);
+            mbar_wait(bar(bars.kv_full), 0, &never);
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        const uint32_t tDV = tmem + kColDV, tDK = tmem + kColDK, tST = tmem + kColST, tDPT = tmem + kColDPT;
+        const uint64_t dKj = make_smem_desc(sK, 16, 8 * 128, kSwizzle128B);
+        const uint64_t dVj = make_smem_desc(sV, 16, 8 * 128, kSwizzle128B);
+        bool ok = n_q == 0 || __all_sync(0xffffffffu, mbar_wait(bar(bars.kv_full), 0, &abort_flag));
+        for (int i = 0; ok && i < n_q; ++i) {
+            const int s = i % kBStages;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t st = sStage + s * kKVStageBytes;
+            const uint64_t dQk = make_smem_desc(st, 16, 8 * 128, kSwizzle128B);                // K-major
+            const uint64_t dDOk = make_smem_desc(st + kTileBytes, 16, 8 * 128, kSwizzle128B);
+            const uint64_t dQm = make_smem_desc(st, kTileElems * 128, 8 * 128, kSwizzle128B);   // MN-major
+            const uint64_t dDOm = make_smem_desc(st + kTileBytes, kTileElems * 128, 8 * 128, kSwizzle128B);
+            if (elect_one_sync()) {
+#pragma unroll
+                for (int kk = 0; kk < kQKSteps; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>((((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128)) >> 4);
+                    mma_f16_ss(tST, dKj + off, dQk + off, kIdesc, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tDPT, dVj + off, dDOk + off, kIdesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(bars.sdp_full));
+            }
+            __syncwarp();
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.p_full), i & 1, &abort_flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (elect_one_sync()) {
+#pragma unroll
+                for (int kk = 0; kk < kDQSteps; ++kk) {
+                    // k-step kk: query columns [16 kk, 16 kk + 16) = token rows of Q_i / dO_i
+                    const uint32_t a = (kk >> 2) * 64 + (kk & 3) * 8;
+                    const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+                    const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+                    mma_f16_ts(tDV, tST + a, dDOm + off, kIdescMN, acc);
+                    mma_f16_ts(tDK, tDPT + a, dQm + off, kIdescMN, acc);
+                }
+                mma_commit(bar(bars.empty[s]));
+                if (i == n_q - 1) mma_commit(bar(bars.final_));
+            }
+            __syncwarp();
+        }
+        if (!ok) {
+            if (elect_one_sync()) {
+                bwd_raise(&abort_flag);
+                mma_commit(bar(bars.drain));
+            }
+            __syncwarp();
+            const volatile int never = 0;
+            mbar_wait(bar(bars.drain), 0, &never);
+        }
+    } else {
+        // ============================================================ P^T, dS^T / epilogue
+        const int quarter = warp & 3;
+        const int half = (warp - 2) >> 2;
+        const int row = quarter * 32 + lane;                   // key row of this thread
+        const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+        const int64_t grow = kv_tile_global * kTileElems + row;
+
+        // this key's position and, per dimension, the query positions whose
+        // window holds it (an interval: window starts grow with the position)
+        int kpos[3];
+        kpos[2] = kc[2] * p.tile[2] + (row & (p.tile[2] - 1));
+        kpos[1] = kc[1] * p.tile[1] + ((row >> p.tlog[2]) & (p.tile[1] - 1));
+        kpos[0] = kc[0] * p.tile[0] + (row >> (p.tlog[1] + p.tlog[2]));
+        int qlo[3], qhi[3];
+#pragma unroll
+        for (int d = 0; d < 3; ++d) {
+            qlo[d] = 1;
+            qhi[d] = 0;                                        // empty unless found
+            if (kpos[d] < p.dims[d]) {
+                for (int q = 0; q < p.dims[d]; ++q) {
+                    const int a = window_start(q, p.dims[d], p.win[d], p.str[d], p.off[d]);
+                    if (a <= kpos[d] && kpos[d] < a + p.win[d]) {
+                        if (qlo[d] > qhi[d]) qlo[d] = q;
+                        qhi[d] = q;
+                    }
+                }
+            }
+        }
+        const float scale_log2 = p.scale * kBLog2e;
+
+        bool ok = true;
+        int qc[3] = {qbox.k0[0], qbox.k0[1], qbox.k0[2]};
+        for (int i = 0; i < n_q && ok; ++i, bwd_odometer(qc, qbox)) {
+            const int s = i % kBStages;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag)) &&
+                 __all_sync(0xffffffffu, mbar_wait(bar(bars.sdp_full), i & 1, &abort_flag));
+            if (!ok) {
+                bwd_raise(&abort_flag);
+                break;
+            }
+            tc_fence_after();
+            // query window of this key in the Q tile's own coordinates
+            int lo[3], span[3];
+            bool full = true;
+#pragma unroll
+            for (int d = 0; d < 3; ++d) {
+                lo[d] = qlo[d] - qc[d] * p.tile[d];
+                span[d] = qhi[d] - qlo[d];                         // negative: empty
+                full = full && lo[d] <= 0 && qhi[d] - qc[d] * p.tile[d] >= p.tile[d] - 1;
+            }
+            const float* lse_s = stage_f + s * (kKVStageBytes / 4) + 2 * (kTileBytes / 4);
+            const float* delta_s = lse_s + kTileElems;
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+                uint32_t rs[32], rp[32];
+                const int col0 = half * 64 + pc * 32;
+                tmem_ld32(tmem + kColST + lane_addr + col0, rs);
+                tmem_ld32(tmem + kColDPT + lane_addr + col0, rp);
+                tmem_wait_ld();
+                bwd_reg_fence(rs);
+                bwd_reg_fence(rp);
+                uint32_t pkp[16], pkd[16];
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    const float4 L4 = *reinterpret_cast<const float4*>(lse_s + col0 + 4 * g4);
+                    const float4 D4 = *reinterpret_cast<const float4*>(delta_s + col0 + 4 * g4);
+                    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
+                    const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
+                    float pv[4], dsv[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int c = col0 + 4 * g4 + e;               // query column of the Q tile
+                        bool valid = full;
+                        if (!full) {
+                            const int cx = c & (p.tile[2] - 1);
+                            const int cy = (c >> p.tlog[2]) & (p.tile[1] - 1);
+                            const int ct = c >> (p.tlog[1] + p.tlog[2]);
+                            valid = static_cast<unsigned>(ct - lo[0]) <= static_cast<unsigned>(span[0]) &&
+                                    static_cast<unsigned>(cy - lo[1]) <= static_cast<unsigned>(span[1]) &&
+                                    static_cast<unsigned>(cx - lo[2]) <= static_cast<unsigned>(span[2]) &&
+                                    span[0] >= 0 && span[1] >= 0 && span[2] >= 0;
+                        }
+                        const int k = 4 * g4 + e;
+                        pv[e] = valid ? bwd_exp2(__uint_as_float(rs[k]) * scale_log2 - Lv[e] * kBLog2e) : 0.0f;
+                        dsv[e] = pv[e] * (__uint_as_float(rp[k]) - Dv[e]);
+                    }
+                    __nv_bfloat162 h0 = __floats2bfloat162_rn(pv[0], pv[1]);
+                    __nv_bfloat162 h1 = __floats2bfloat162_rn(pv[2], pv[3]);
+                    __nv_bfloat162 g0 = __floats2bfloat162_rn(dsv[0], dsv[1]);
+                    __nv_bfloat162 g1 = __floats2bfloat162_rn(dsv[2], dsv[3]);
+                    pkp[2 * g4] = *reinterpret_cast<uint32_t*>(&h0);
+                    pkp[2 * g4 + 1] = *reinterpret_cast<uint32_t*>(&h1);
+                    pkd[2 * g4] = *reinterpret_cast<uint32_t*>(&g0);
+                    pkd[2 * g4 + 1] = *reinterpret_cast<uint32_t*>(&g1);
+                }
+                tmem_st16(tmem + kColST + lane_addr + half * 64 + pc * 16, pkp);
+                tmem_st16(tmem + kColDPT + lane_addr + half * 64 + pc * 16, pkd);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars.p_full));
+        }
+
+        // ------------------------------------------------------------ epilogue
+        if (ok && n_q > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.final_), 0, &abort_flag));
+            if (!ok) bwd_raise(&abort_flag);
+        }
+        if (ok) {
+            tc_fence_after();
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {              // 0: dv, 1: dk (times scale)
+                uint8_t* dst_row = static_cast<uint8_t*>(which == 0 ? p.dv : p.dk) + grow * kRowBytes +
+                                   half * (kRowBytes / 2);
+                const float mul = which == 0 ? 1.0f : p.scale;
+#pragma unroll
+                for (int pc = 0; pc < 2; ++pc) {
+                    uint32_t r[32];
+                    if (n_q > 0) {
+                        tmem_ld32(tmem + (which == 0 ? kColDV : kColDK) + lane_addr + half * 64 + pc * 32, r);
+                        tmem_wait_ld();
+                        bwd_reg_fence(r);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) r[i] = 0u;     // no query reaches this key tile
+                    }
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * mul,
+                                                                 __uint_as_float(r[2 * i + 1]) * mul);
+                        pk[i] = *reinterpret_cast<uint32_t*>(&h);
+                    }
+                    uint4* dst = reinterpret_cast<uint4*>(dst_row + pc * 64);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kBTmemCols);
+    }
+}
+
 // delta_i = <dout_i, out_i> (fp32 accumulation of the bf16 rows), one warp per
 // tiled row: 128 elements, 4 per lane.
 __global__ void gna_bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
@@ -428,6 +788,16 @@ cudaError_t launch_backward_dq(const BwdParams& p, int64_t num_q_tiles, cudaStre
     cudaError_t e = cudaFuncSetAttribute(gna_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
     if (e != cudaSuccess) return e;
     gna_bwd_dq_kernel<<<dim3(static_cast<unsigned>(num_q_tiles)), kBThreads, kSmemAlloc, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_backward_dkdv(const BwdKVParams& p, int64_t num_kv_tiles, cudaStream_t stream)
+{
+    if (num_kv_tiles <= 0) return cudaSuccess;
+    cudaError_t e =
+        cudaFuncSetAttribute(gna_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKVSmemAlloc);
+    if (e != cudaSuccess) return e;
+    gna_bwd_dkdv_kernel<<<dim3(static_cast<unsigned>(num_kv_tiles)), kBThreads, kKVSmemAlloc, stream>>>(p);
     return cudaGetLastError();
 }
 

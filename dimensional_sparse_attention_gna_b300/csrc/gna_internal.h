@@ -71,6 +71,25 @@ struct BwdParams {
     float scale;
 };
 
+// Parameters of one dK / dV launch of the backward pass (bf16, head_dim 128,
+// all tensors tiled).
+struct BwdKVParams {
+    CUtensorMap tmQ;             // 2-D TMA views [rows, 128] of the tiled q, dout, k and v
+    CUtensorMap tmDO;
+    CUtensorMap tmK;
+    CUtensorMap tmV;
+    const float* lse;            // tiled lse [rows] of the forward (natural log)
+    const float* delta;          // tiled <dout, out> [rows]
+    void* dk;                    // tiled bf16 dk [rows, 128]
+    void* dv;                    // tiled bf16 dv [rows, 128]
+    int dims[3], win[3], str[3], off[3];
+    int tile[3], tlog[3], nt[3];
+    int tiles_per_head;
+    float scale;
+};
+
+cudaError_t launch_backward_dkdv(const BwdKVParams& p, int64_t num_kv_tiles, cudaStream_t stream);
+
 // dQ over num_q_tiles CTAs, and delta = <dout, out> over `rows` tiled rows.
 cudaError_t launch_backward_dq(const BwdParams& p, int64_t num_q_tiles, cudaStream_t stream);
 cudaError_t launch_backward_delta(const void* out, const void* dout, float* delta, int64_t rows,

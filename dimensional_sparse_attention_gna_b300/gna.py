@@ -98,6 +98,9 @@ def lib() -> ctypes.CDLL:
         L.gna_backward_dq.restype = st
         L.gna_backward_dq.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _INT,
                                       ctypes.POINTER(GNAOptions), _P]
+        L.gna_backward_dkdv.restype = st
+        L.gna_backward_dkdv.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _INT,
+                                        ctypes.POINTER(GNAOptions), _P]
         L.gna_tile_stats.restype = st
         L.gna_tile_stats.argtypes = [_I3, _I3, _I3, _P, _INT, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
@@ -359,6 +362,29 @@ def gna_backward_dq(q: torch.Tensor, k: torch.Tensor, k_value: torch.Tensor, v: 
     _check(lib().gna_backward_dq(_ptr(q), _ptr(k), _ptr(k_value), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta),
                                  _ptr(dq), B, heads, _I3(*dims), _I3(*window), _I3(*stride), head_dim, GNA_BF16,
                                  ctypes.byref(opt), _stream_ptr(stream)))
+
+
+def gna_backward_dkdv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor,
+                      delta: torch.Tensor, dk: torch.Tensor, dv: torch.Tensor, B: int, heads: int, dims, window,
+                      stride, head_dim: int, *, tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0,
+                      stream=None):
+    """dk and dv of the GNA forward (see ``include/gna.h``): tiled bf16 tensors,
+    the forward's tiled ``lse`` and ``delta`` from :func:`gna_backward_delta`."""
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout), ("dk", dk), ("dv", dv)):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+    if lse.dtype != torch.float32 or delta.dtype != torch.float32:
+        raise ValueError("lse and delta must be float32")
+    nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
+    _need(q=(q, nt), k=(k, nt), v=(v, nt), dout=(dout, nt), dk=(dk, nt), dv=(dv, nt), lse=(lse, nt // head_dim),
+          delta=(delta, nt // head_dim))
+    opt = GNAOptions()
+    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+    opt.leader_rule = leader_rule
+    opt.scale = scale
+    _check(lib().gna_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dk),
+                                   _ptr(dv), B, heads, _I3(*dims), _I3(*window), _I3(*stride), head_dim, GNA_BF16,
+                                   ctypes.byref(opt), _stream_ptr(stream)))
 
 
 def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADER_CENTER):

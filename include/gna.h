@@ -206,12 +206,23 @@ gna_status gna_forward_raster(const void* q, const void* k, const void* v, void*
  *   lse           : the forward's tiled lse; delta: from gna_backward_delta
  *   dq            : tiled bfloat16, written (padding rows zero)
  *   window, stride, opt : as given to the forward
+ *
+ * gna_backward_dkdv: dv_j = sum_{i : j in N(i)} p_ij dout_i and
+ * dk_j = scale sum_{i : j in N(i)} p_ij (<dout_i, v_j> - delta_i) q_i: one CTA
+ * per KV tile walks the Q tiles whose windows reach it.
+ *   q, k, v, dout : tiled bfloat16; lse, delta as for gna_backward_dq
+ *   dk, dv        : tiled bfloat16, written (padding rows zero)
+ *
  * Asynchronous on `stream`; a kernel that abandons a wait reports through
  * gna_get_status.  GNA_ERR_UNSUPPORTED for other dtypes or head_dims,
- * GNA_ERR_INVALID_ARG as gna_forward_ex.  dk and dv are not computed yet. */
+ * GNA_ERR_INVALID_ARG as gna_forward_ex. */
 gna_status gna_backward_delta(const void* out, const void* dout, float* delta, int B, int heads,
                               const int dims[3], int head_dim, gna_dtype dtype, const gna_options* opt,
                               void* stream);
+gna_status gna_backward_dkdv(const void* q, const void* k, const void* v, const void* dout, const float* lse,
+                             const float* delta, void* dk, void* dv, int B, int heads, const int dims[3],
+                             const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
+                             const gna_options* opt, void* stream);
 gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, const void* v,
                            const void* dout, const float* lse, const float* delta, void* dq, int B,
                            int heads, const int dims[3], const int window[3], const int stride[3],

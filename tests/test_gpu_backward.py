@@ -1,10 +1,12 @@
-"""dQ of the CUDA backward (``gna_backward_delta`` + ``gna_backward_dq``) against
-the pinned backward oracle, every element compared.
+"""The CUDA backward (``gna_backward_delta``, ``gna_backward_dq``,
+``gna_backward_dkdv``) against the pinned backward oracle, every element of dq,
+dk and dv compared.
 
 The GPU path reads the bf16 out and lse of its own forward; the oracle
 recomputes everything in float64 from the same bf16 inputs.  The differences
 come from bf16 dS, bf16 out in delta and the bf16 result, so the bar is a
-relative one: relative RMS < 2e-2 and max |error| <= 5 % of max |dq|.
+relative one: relative RMS < 1e-2 and max |error| <= 2 % of max |gradient|
+(measured: relative RMS ~2.4e-3, max |error| ~0.5 %, the size of bf16 rounding).
 """
 import numpy as np
 import pytest
@@ -17,7 +19,8 @@ from synthetic_inputs import exact_f32, normal_raster, to_bf16
 pytestmark = pytest.mark.gpu
 
 
-def gpu_dq(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
+def gpu_backward(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
+    """(dq, dk, dv) raster float32 and the tiled bf16 results, through the C ABI."""
     B, T, H, W, heads, d = q.shape
     dev = torch.device("cuda")
     shp = G.tiled_shape(B, heads, dims, d, tile)
@@ -39,27 +42,34 @@ def gpu_dq(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEADER_CEN
     dq_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
     G.gna_backward_dq(tiled["q"], tiled["k"], k_val, tiled["v"], tiled["dout"], lse_t, delta, dq_t, B, heads, dims,
                       window, stride, d, tile=tile, leader_rule=rule)
-    dq = torch.empty((B,) + tuple(dims) + (heads, d), dtype=torch.bfloat16, device=dev)
-    G.gna_unpermute(dq_t, dq, B, heads, dims, d, tile=tile)
+    dk_t, dv_t = (torch.empty(shp, dtype=torch.bfloat16, device=dev) for _ in range(2))
+    G.gna_backward_dkdv(tiled["q"], tiled["k"], tiled["v"], tiled["dout"], lse_t, delta, dk_t, dv_t, B, heads, dims,
+                        window, stride, d, tile=tile, leader_rule=rule)
+    res = []
+    for t in (dq_t, dk_t, dv_t):
+        r = torch.empty((B,) + tuple(dims) + (heads, d), dtype=torch.bfloat16, device=dev)
+        G.gna_unpermute(t, r, B, heads, dims, d, tile=tile)
+        res.append(r)
     G.gna_get_status()
     torch.cuda.synchronize()
-    return dq.float().cpu().numpy(), dq_t
+    return [r.float().cpu().numpy() for r in res], (dq_t, dk_t, dv_t)
 
 
-def _check_dq(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
+def _check_grads(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
     d = 128
     q, k, v, dout = (to_bf16(normal_raster(seed + i, B, dims, heads, d)) for i in range(4))
-    dq, _ = gpu_dq(q, k, v, dout, dims, window, stride, tile=tile, rule=rule)
+    got, _ = gpu_backward(q, k, v, dout, dims, window, stride, tile=tile, rule=rule)
     orule = oracle.LEADER_CENTER if rule == G.GNA_LEADER_CENTER else oracle.LEADER_LITERAL
-    dq_ref, _, _ = oracle.backward_c(exact_f32(q), exact_f32(k), exact_f32(v), exact_f32(dout), dims, window,
-                                     stride, rule=orule)
-    err = np.abs(dq.astype(np.float64) - dq_ref)
-    rel = float(np.sqrt((err ** 2).mean() / (dq_ref ** 2).mean()))
-    info = f"max|err|={err.max():.3e} max|dq|={np.abs(dq_ref).max():.3e} relRMS={rel:.3e}"
-    assert np.isfinite(dq).all(), info
-    assert rel < 2e-2, info
-    assert err.max() <= 0.05 * np.abs(dq_ref).max(), info
-    return rel
+    refs = oracle.backward_c(exact_f32(q), exact_f32(k), exact_f32(v), exact_f32(dout), dims, window, stride,
+                             rule=orule)
+    for name, g, r in zip(("dq", "dk", "dv"), got, refs):
+        err = np.abs(g.astype(np.float64) - r)
+        rel = float(np.sqrt((err ** 2).mean() / (r ** 2).mean()))
+        info = f"{name}: max|err|={err.max():.3e} max|ref|={np.abs(r).max():.3e} relRMS={rel:.3e}"
+        print(info)
+        assert np.isfinite(g).all(), info
+        assert rel < 1e-2, info
+        assert err.max() <= 0.02 * np.abs(r).max(), info
 
 
 @pytest.mark.parametrize("B,heads,dims,window,stride,tile,rule", [
@@ -71,18 +81,19 @@ def _check_dq(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER
     (1, 2, (2, 8, 16), (2, 8, 16), (1, 1, 1), None, G.GNA_LEADER_CENTER),      # window = grid
     (1, 2, (4, 16, 16), (2, 8, 8), (2, 8, 8), None, G.GNA_LEADER_CENTER),      # blocked
 ])
-def test_dq_small_grids_all_elements(B, heads, dims, window, stride, tile, rule):
-    _check_dq(8000 + sum(dims), B, heads, dims, window, stride, tile=tile, rule=rule)
+def test_gradients_small_grids_all_elements(B, heads, dims, window, stride, tile, rule):
+    _check_grads(8000 + sum(dims), B, heads, dims, window, stride, tile=tile, rule=rule)
 
 
-def test_dq_mid_size_video_grid():
+def test_gradients_mid_size_video_grid():
     """Several KV tiles per dimension and full interior tiles (8x24x40 tokens, 4 heads)."""
-    _check_dq(8100, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1))
+    _check_grads(8100, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1))
 
 
-def test_dq_repeat_runs_bit_identical():
+def test_gradients_repeat_runs_bit_identical():
     dims, window, stride, d = (4, 16, 24), (3, 9, 11), (1, 2, 3), 128
     q, k, v, dout = (to_bf16(normal_raster(8200 + i, 1, dims, 2, d)) for i in range(4))
-    _, a = gpu_dq(q, k, v, dout, dims, window, stride)
-    _, b = gpu_dq(q, k, v, dout, dims, window, stride)
-    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    _, a = gpu_backward(q, k, v, dout, dims, window, stride)
+    _, b = gpu_backward(q, k, v, dout, dims, window, stride)
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
