@@ -62,6 +62,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--sustain", type=float, default=0.0,
                     help="also run the forward back to back for this many seconds and report the sustained rate")
+    ap.add_argument("--backward", action="store_true",
+                    help="also time the backward pass (delta, dq, dk/dv kernels; bf16, head_dim 128, tiled layout)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
@@ -512,6 +514,50 @@ def gpu_arm(a, rank, world, local):
         sustained = {"value": flops_rank / (sus_ms / 1e3) / 1e12, "unit": "TFLOP/s", "launches": n_sus,
                      "forward_ms": sus_ms, "seconds": a.sustain, "clocks": sclk.summary(),
                      "frac_of_sustained_peak": flops_rank / (sus_ms / 1e3) / 1e12 / peak_sustained}
+    # optional: the backward pass on the same workload, inputs resident (tiled
+    # q, k, v, dout; k in the value layout; the forward's out and lse)
+    backward = None
+    if a.backward and a.dtype == "bf16" and d == 128 and not raster:
+        v_tiled = torch.empty(shp, dtype=dt, device=dev)
+        k_val = torch.empty_like(vt)
+        G.gna_permute(xs[2], v_tiled, B, heads, dims, d, stream=stream)
+        G.gna_permute_v(xs[1], k_val, B, heads, dims, d, stream=stream)
+        dout_t = torch.randn(shp, device=dev, generator=gen, dtype=torch.float32).to(dt)
+        delta = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
+        dq_t, dk_t, dv_t = (torch.empty(shp, dtype=dt, device=dev) for _ in range(3))
+        G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, a.window, a.stride, d, stream=stream)
+
+        def bwd(ev3=None):
+            if ev3:
+                ev3[0].record(stream)
+            G.gna_backward_delta(out_t, dout_t, delta, B, heads, dims, d, stream=stream)
+            G.gna_backward_dq(qt, kt, k_val, v_tiled, dout_t, lse_t, delta, dq_t, B, heads, dims, a.window, a.stride,
+                              d, stream=stream)
+            if ev3:
+                ev3[1].record(stream)
+            G.gna_backward_dkdv(qt, kt, v_tiled, dout_t, lse_t, delta, dk_t, dv_t, B, heads, dims, a.window,
+                                a.stride, d, stream=stream)
+            if ev3:
+                ev3[2].record(stream)
+        for _ in range(2):
+            bwd()
+        runs = []
+        for _ in range(3):
+            ev3 = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+            bwd(ev3)
+            runs.append(ev3)
+        torch.cuda.synchronize()
+        G.gna_get_status(stream)
+        dq_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in runs)
+        dkdv_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in runs)
+        bwd_ms = dq_ms + dkdv_ms
+        # five window-restricted matmuls (S, dP, dV, dK, dQ), 2 flops per MAC
+        bwd_flops = 2.5 * flops_rank
+        backward = {"ms": bwd_ms, "useful_tflops": bwd_flops / (bwd_ms / 1e3) / 1e12,
+                    "frac_of_burst_peak": bwd_flops / (bwd_ms / 1e3) / 1e12 / peak_burst,
+                    "kernels_ms": {"delta_and_dq": dq_ms, "dk_dv": dkdv_ms},
+                    "flops": "10 * B * heads * N * |window| * d (S, dP, dV, dK, dQ restricted to the window)"}
+        del v_tiled, k_val, dout_t, delta, dq_t, dk_t, dv_t
     traffic = kernel_traffic(a)
 
     cpu = None
@@ -552,7 +598,7 @@ def gpu_arm(a, rank, world, local):
         "speedup_bound_at_equal_tile_rate": G.gna_plan_tile(dims, a.window, a.stride)[2],
         "speedup_over_ratio": None if speedup is None else speedup / n_ratio,
         "e2e": e2e, "gpu_launches": launches_per_step * a.steps, "clocks": clk, "cpu_baseline": cpu,
-        "sustained": sustained,
+        "sustained": sustained, "backward": backward,
     }
     print(json.dumps(line), flush=True)
 
