@@ -656,6 +656,8 @@ gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, co
     p.lse = lse;
     p.delta = delta;
     p.dq = dq;
+    p.fault_skip_kv = -1;
+    if (const char* f = std::getenv("GNA_TEST_SKIP_BWD_LOAD")) p.fault_skip_kv = std::atoi(f);
     const int64_t rows = nq * gna::kTileElems;
     if ((st = make_tile_map(&p.tmK, k, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_tile_map(&p.tmV, v, rows, head_dim, 2)) != GNA_OK) return st;

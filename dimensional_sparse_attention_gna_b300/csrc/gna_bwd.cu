@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
                 early = true;
                 break;
             }
+            if (j == p.fault_skip_kv) { early = true; break; }   // test hook: consumers wait in vain
             if (elect_one_sync()) {
                 const uint32_t st = s_base + s * kStageBytes;
                 mbar_arrive_expect_tx(bar(bars.full[s]), kStageBytes);
@@ -198,7 +199,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             ++issued;
         }
         if (early) {
-            if (lane == 0) bwd_raise(&abort_flag);
+            // a skipped load (test hook) is left for the consumers' waits to find
+            if (p.fault_skip_kv < 0 && lane == 0) bwd_raise(&abort_flag);
             const volatile int never = 0;
             for (int j = (issued > kBStages ? issued - kBStages : 0); j < issued; ++j)
                 mbar_wait(bar(bars.full[j % kBStages]), (j / kBStages) & 1, &never);

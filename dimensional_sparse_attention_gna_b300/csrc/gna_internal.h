@@ -69,6 +69,7 @@ struct BwdParams {
     int tile[3], tlog[3], nt[3];
     int tiles_per_head;
     float scale;
+    int fault_skip_kv;           // test hook: >= 0 makes the producer skip that KV load
 };
 
 // Parameters of one dK / dV launch of the backward pass (bf16, head_dim 128,
