@@ -8,6 +8,8 @@
 * stride = window on a divisible grid: the same, block by block;
 * window 1: out = v exactly, so dv = dout and dq = dk = 0;
 * the C and the loop versions agree on random cases;
+* three identities of the derivative that hold at any size (sums of dv and dk,
+  and sum <dq, q> = sum <dk, k>);
 * planted mistakes in the softmax Jacobian are caught by the finite differences.
 """
 import itertools
@@ -117,6 +119,25 @@ def test_c_backward_equals_loops(dims, window, stride, rule):
         np.testing.assert_allclose(g, w, rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("dims,window,stride,rule", [
+    ((3, 6, 7), (2, 3, 5), (1, 2, 3), ref.LEADER_CENTER),
+    ((2, 8, 9), (2, 4, 4), (2, 4, 4), ref.LEADER_LITERAL),
+])
+def test_backward_identities(dims, window, stride, rule):
+    """Identities of the derivative, true at any size:
+    sum_j dv_j = sum_i dout_i (each query's probabilities sum to 1);
+    sum_j dk_j = 0 (each query's row of dS sums to 0);
+    sum_i <dq_i, q_i> = sum_j <dk_j, k_j> (both are sum_ij ds_ij s_ij)."""
+    q, k, v, dout = _inputs(26, 2, dims, 3, 8)
+    dq, dk, dv = ref.gna_backward_loops(q, k, v, dout, dims, window, stride, rule=rule)
+    axes = (1, 2, 3)                                   # the grid; per batch, head and feature
+    np.testing.assert_allclose(dv.sum(axis=axes), dout.sum(axis=axes), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(dk.sum(axis=axes), 0.0, rtol=0, atol=1e-10)
+    lhs = (dq * q).sum(axis=(1, 2, 3, 5))
+    rhs = (dk * k).sum(axis=(1, 2, 3, 5))
+    np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-10)
+
+
 def _jac_no_centering(p, dp):
     return p * dp
 
@@ -131,5 +152,8 @@ def _jac_mean_centering(p, dp):
 
 @pytest.mark.parametrize("mutant", [_jac_no_centering, _jac_no_p_factor, _jac_mean_centering])
 def test_planted_jacobian_mistakes_are_caught(monkeypatch, mutant):
+    """Each slip fails the finite differences, and the identities as well."""
     monkeypatch.setattr(ref, "softmax_backward", mutant)
     assert _fd_errors((2, 5, 6), (2, 3, 3), (1, 1, 1), ref.LEADER_CENTER, seed=11) > 1e-4
+    with pytest.raises(AssertionError):
+        test_backward_identities((3, 6, 7), (2, 3, 5), (1, 2, 3), ref.LEADER_CENTER)
