@@ -520,6 +520,24 @@ gna_status gna_forward_raster(const void* q, const void* k, const void* v, void*
     return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, true);
 }
 
+gna_status gna_schedule_step(int step, int num_steps, int full_steps, const int dims[3], const int window[3],
+                             const int stride[3], int out_window[3], int out_stride[3])
+{
+    if (out_window == nullptr || out_stride == nullptr) return fail(GNA_ERR_INVALID_ARG, "output is NULL");
+    if (!(0 <= step && step < num_steps)) return fail(GNA_ERR_INVALID_ARG, "need 0 <= step < num_steps");
+    if (!(0 <= full_steps && full_steps <= num_steps))
+        return fail(GNA_ERR_INVALID_ARG, "need 0 <= full_steps <= num_steps");
+    gna_status st = check_geometry(dims, window, stride);
+    if (st != GNA_OK) return st;
+    const bool full = step < full_steps;
+    for (int d = 0; d < 3; ++d) {
+        out_window[d] = full ? dims[d] : window[d];
+        out_stride[d] = full ? 1 : stride[d];
+    }
+    t_last_error.clear();
+    return GNA_OK;
+}
+
 gna_status gna_get_status(void* stream)
 {
     int status = 0, bwd_status = 0;

@@ -107,6 +107,8 @@ def lib() -> ctypes.CDLL:
         L.gna_plan_tile.restype = st
         L.gna_plan_tile.argtypes = [_I3, _I3, _I3, _INT, _I3, ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_double)]
+        L.gna_schedule_step.restype = st
+        L.gna_schedule_step.argtypes = [_INT, _INT, _INT, _I3, _I3, _I3, _I3, _I3]
         L.gna_get_status.restype = st
         L.gna_get_status.argtypes = [_P]
         _lib = L
@@ -385,6 +387,14 @@ def gna_backward_dkdv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: t
     _check(lib().gna_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dk),
                                    _ptr(dv), B, heads, _I3(*dims), _I3(*window), _I3(*stride), head_dim, GNA_BF16,
                                    ctypes.byref(opt), _stream_ptr(stream)))
+
+
+def gna_schedule_step(step: int, num_steps: int, full_steps: int, dims, window, stride):
+    """(window, stride) for diffusion step ``step``: the whole grid with stride 1
+    (full attention) for the first ``full_steps`` steps, then ``window``/``stride``."""
+    w, s_ = _I3(), _I3()
+    _check(lib().gna_schedule_step(step, num_steps, full_steps, _I3(*dims), _I3(*window), _I3(*stride), w, s_))
+    return tuple(w), tuple(s_)
 
 
 def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADER_CENTER):

@@ -255,6 +255,18 @@ gna_status gna_tile_stats(const int dims[3], const int window[3], const int stri
 gna_status gna_plan_tile(const int dims[3], const int window[3], const int stride[3], int leader_rule,
                          int tile[3], double* tile_overhead, double* speedup_bound);
 
+/* Step schedule of a diffusion sampler.  The GNA page keeps full attention for
+ * the first steps and switches to GNA afterwards: §3.2 runs the first 9 of 28
+ * FLUX steps with full attention, §4.2 advises full attention for the first
+ * 10-20 % of the steps, §5 larger windows early.  Full attention is GNA with
+ * window = grid and stride 1 (the forward then visits every KV tile).  For step
+ * `step` (0-based) of `num_steps`, writes the window and stride to pass to the
+ * forward: the whole grid with stride 1 while step < full_steps, else `window`
+ * and `stride`.  Host only.  GNA_ERR_INVALID_ARG unless 0 <= step < num_steps,
+ * 0 <= full_steps <= num_steps and the geometry is valid. */
+gna_status gna_schedule_step(int step, int num_steps, int full_steps, const int dims[3], const int window[3],
+                             const int stride[3], int out_window[3], int out_stride[3]);
+
 /* ------------------------------------------------------------ status ---- */
 
 /* Synchronises `stream`, then returns and clears the device status word

@@ -270,3 +270,28 @@ def test_backward_rejects_bad_arguments_on_host(L):
     assert L.gna_backward_delta(FAKE, FAKE + 8, FAKE, 1, 2, dims, 128, G.GNA_BF16, None, None) == \
         G.GNA_ERR_INVALID_ARG
     assert L.gna_backward_delta(FAKE, FAKE, FAKE, 0, 2, dims, 128, G.GNA_BF16, None, None) == G.GNA_ERR_INVALID_ARG
+
+
+def test_schedule_step_full_attention_first():
+    """GNA page §3.2: 28 steps, the first 9 with full attention, then GNA s16x16."""
+    dims, window, stride = (1, 256, 256), (1, 64, 64), (1, 16, 16)
+    got = [G.gna_schedule_step(i, 28, 9, dims, window, stride) for i in range(28)]
+    assert all(g == (dims, (1, 1, 1)) for g in got[:9])
+    assert all(g == (window, stride) for g in got[9:])
+    # no full steps / all full steps
+    assert G.gna_schedule_step(0, 28, 0, dims, window, stride) == (window, stride)
+    assert G.gna_schedule_step(27, 28, 28, dims, window, stride) == (dims, (1, 1, 1))
+    # full attention is a valid GNA geometry, and visits every KV tile
+    w, s = G.gna_schedule_step(0, 28, 9, dims, window, stride)
+    v, p_, q = G.gna_tile_stats(dims, w, s)
+    assert v == q * q and p_ == 0
+
+
+@pytest.mark.parametrize("args", [
+    (28, 28, 9), (-1, 28, 9), (0, 28, 29), (0, 28, -1), (0, 0, 0),
+])
+def test_schedule_step_rejects_bad_steps(args):
+    with pytest.raises(G.GNAError):
+        G.gna_schedule_step(*args, (1, 16, 16), (1, 5, 5), (1, 1, 1))
+    with pytest.raises(G.GNAError):
+        G.gna_schedule_step(0, 28, 9, (1, 16, 16), (1, 17, 5), (1, 1, 1))
