@@ -310,3 +310,110 @@ int gna_oracle_backward(const float *q, const float *k, const float *v, const fl
     free(th);
     return rc;
 }
+
+/*
+ * dq of selected queries (the same derivative as gna_oracle_backward; dq_i
+ * depends only on query i's own window, so a sample costs O(|W| d) per query).
+ * sel: flat query ids ((b*heads + h)*N + (t*H + y)*W + x); dq: double [nsel, d].
+ */
+typedef struct {
+    const bjob_t *J;
+    const int64_t *sel;
+    int64_t begin, end;
+    double *dq;
+    int status;
+} dqjob_t;
+
+static void *dq_worker(void *arg)
+{
+    dqjob_t *Q = (dqjob_t *)arg;
+    const bjob_t *J = Q->J;
+    const int T = J->dims[0], H = J->dims[1], W = J->dims[2], d = J->d;
+    const int64_t N = (int64_t)T * H * W;
+    int64_t wsz = (int64_t)J->win[0] * J->win[1] * J->win[2];
+    double *pbuf = (double *)malloc(sizeof(double) * (size_t)wsz);
+    double *dpbuf = (double *)malloc(sizeof(double) * (size_t)wsz);
+    if (!pbuf || !dpbuf) { free(pbuf); free(dpbuf); Q->status = -2; return NULL; }
+    for (int64_t r = Q->begin; r < Q->end; ++r) {
+        const int64_t flat = Q->sel[r];
+        const int64_t tok = flat % N, bh = flat / N;
+        const int h = (int)(bh % J->heads), b = (int)(bh / J->heads);
+        const int x = (int)(tok % W), y = (int)((tok / W) % H), t = (int)(tok / ((int64_t)W * H));
+        const int a0 = start_of(t, T, J->win[0], J->str[0], J->rule);
+        const int a1 = start_of(y, H, J->win[1], J->str[1], J->rule);
+        const int a2 = start_of(x, W, J->win[2], J->str[2], J->rule);
+        const int64_t qi = row_of(J, b, t, y, x, h) * d;
+        int64_t n = 0;
+        double m = -INFINITY;
+        for (int kt = a0; kt < a0 + J->win[0]; ++kt)
+            for (int ky = a1; ky < a1 + J->win[1]; ++ky)
+                for (int kx = a2; kx < a2 + J->win[2]; ++kx) {
+                    const int64_t kj = row_of(J, b, kt, ky, kx, h) * d;
+                    double acc = 0.0, dacc = 0.0;
+                    for (int c = 0; c < d; ++c) {
+                        acc += (double)J->q[qi + c] * (double)J->k[kj + c];
+                        dacc += (double)J->dout[qi + c] * (double)J->v[kj + c];
+                    }
+                    pbuf[n] = J->scale * acc;
+                    dpbuf[n] = dacc;
+                    if (pbuf[n] > m) m = pbuf[n];
+                    ++n;
+                }
+        double z = 0.0, dsum = 0.0;
+        for (int64_t l = 0; l < n; ++l) { pbuf[l] = exp(pbuf[l] - m); z += pbuf[l]; }
+        for (int64_t l = 0; l < n; ++l) { pbuf[l] /= z; dsum += pbuf[l] * dpbuf[l]; }
+        double *o = Q->dq + r * d;
+        for (int c = 0; c < d; ++c) o[c] = 0.0;
+        n = 0;
+        for (int kt = a0; kt < a0 + J->win[0]; ++kt)
+            for (int ky = a1; ky < a1 + J->win[1]; ++ky)
+                for (int kx = a2; kx < a2 + J->win[2]; ++kx) {
+                    const int64_t kj = row_of(J, b, kt, ky, kx, h) * d;
+                    const double ds = pbuf[n] * (dpbuf[n] - dsum);
+                    ++n;
+                    for (int c = 0; c < d; ++c) o[c] += J->scale * ds * (double)J->k[kj + c];
+                }
+    }
+    free(pbuf);
+    free(dpbuf);
+    return NULL;
+}
+
+int gna_oracle_backward_dq_sel(const float *q, const float *k, const float *v, const float *dout,
+                               int B, int heads, const int dims[3], const int window[3],
+                               const int stride[3], int head_dim, int rule, double scale,
+                               const int64_t *sel, int64_t nsel, double *dq, int nthreads)
+{
+    if (B < 1 || heads < 1 || head_dim < 1 || (rule != 0 && rule != 1) || !sel || nsel < 0) return -1;
+    for (int i = 0; i < 3; ++i)
+        if (!(1 <= stride[i] && stride[i] <= window[i] && window[i] <= dims[i])) return -1;
+    const int64_t total = (int64_t)B * heads * dims[0] * dims[1] * dims[2];
+    for (int64_t r = 0; r < nsel; ++r)
+        if (sel[r] < 0 || sel[r] >= total) return -1;
+    bjob_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.dout = dout;
+    J.B = B; J.heads = heads; J.d = head_dim; J.rule = rule; J.scale = scale;
+    for (int c = 0; c < 3; ++c) { J.dims[c] = dims[c]; J.win[c] = window[c]; J.str[c] = stride[c]; }
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > nsel) nthreads = nsel > 0 ? (int)nsel : 1;
+    dqjob_t *jobs = (dqjob_t *)calloc((size_t)nthreads, sizeof(dqjob_t));
+    pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    if (!jobs || !th) { free(jobs); free(th); return -2; }
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i].J = &J; jobs[i].sel = sel; jobs[i].dq = dq;
+        jobs[i].begin = nsel * i / nthreads;
+        jobs[i].end = nsel * (i + 1) / nthreads;
+    }
+    int rc = 0;
+    if (nthreads == 1) {
+        dq_worker(&jobs[0]);
+    } else {
+        for (int i = 0; i < nthreads; ++i) pthread_create(&th[i], NULL, dq_worker, &jobs[i]);
+        for (int i = 0; i < nthreads; ++i) pthread_join(th[i], NULL);
+    }
+    for (int i = 0; i < nthreads; ++i) if (jobs[i].status) rc = jobs[i].status;
+    free(jobs);
+    free(th);
+    return rc;
+}

@@ -7,7 +7,8 @@
   autograd in float64 (a library routine);
 * stride = window on a divisible grid: the same, block by block;
 * window 1: out = v exactly, so dv = dout and dq = dk = 0;
-* the C and the loop versions agree on random cases;
+* the C and the loop versions agree on random cases, and the selected-query dq
+  of the C oracle equals its whole-plane dq;
 * three identities of the derivative that hold at any size (sums of dv and dk,
   and sum <dq, q> = sum <dk, k>);
 * planted mistakes in the softmax Jacobian are caught by the finite differences.
@@ -136,6 +137,17 @@ def test_backward_identities(dims, window, stride, rule):
     lhs = (dq * q).sum(axis=(1, 2, 3, 5))
     rhs = (dk * k).sum(axis=(1, 2, 3, 5))
     np.testing.assert_allclose(lhs, rhs, rtol=0, atol=1e-10)
+
+
+def test_selected_query_dq_matches_whole_planes():
+    dims, window, stride = (3, 6, 7), (2, 3, 5), (1, 2, 3)
+    q, k, v, dout = (x.astype(np.float32) for x in _inputs(27, 2, dims, 3, 8))
+    dq, _, _ = oracle.backward_c(q, k, v, dout, dims, window, stride, threads=2)
+    rng = np.random.default_rng(27)
+    sel = np.array([tuple(int(rng.integers(0, n)) for n in (2, 3) + dims) for _ in range(40)])
+    ids = oracle.query_ids(sel[:, 0], sel[:, 1], sel[:, 2], sel[:, 3], sel[:, 4], 3, dims)
+    got = oracle.backward_dq_c(q, k, v, dout, dims, window, stride, ids, threads=3)
+    np.testing.assert_allclose(got, dq[sel[:, 0], sel[:, 2], sel[:, 3], sel[:, 4], sel[:, 1]], rtol=0, atol=1e-12)
 
 
 def _jac_no_centering(p, dp):
