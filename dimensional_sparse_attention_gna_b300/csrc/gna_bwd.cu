@@ -1,4 +1,5 @@
-// Backward pass of the GNA forward for sm_103a: dQ and the per-query delta.
+// Backward pass of the GNA forward for sm_103a: the per-query delta, dQ (one CTA
+// per Q tile, below) and dK / dV (one CTA per KV tile, further down).
 //
 // GNA page ("GNA稀疏注意力机制：视觉Transformer计算优化实践") §4.2, problem 1
 // and §5 ask for GNA in training; the page gives no backward, so this is the

@@ -1,6 +1,7 @@
 /*
  * gna.h -- C ABI of the B300 (sm_103a) Generalized Neighborhood Attention
- * forward library (libgna_b300.so).
+ * library (libgna_b300.so): the forward pass with its layout permutes, a
+ * backward pass (bf16, head_dim 128) and host-side planning.
  *
  * What the library computes
  * -------------------------
