@@ -13,8 +13,9 @@ Contents
 * ``gna_oracle.c``        -- the same definition in plain C, threaded over
   queries, float64 accumulation; wrapped here by :func:`forward_c`; and its
   derivative (the backward pass), threaded over (b, head) planes, wrapped by
-  :func:`backward_c`, and its dq at selected queries (:func:`backward_dq_c`),
-  cheap enough for samples of the full-size workloads.
+  :func:`backward_c`, its dq at selected queries (:func:`backward_dq_c`) and its
+  dk, dv at selected keys (:func:`backward_kv_c`), cheap enough for samples of
+  the full-size workloads.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` (the backward by
 ``tests/test_oracle_backward_pins.py``) against hand-derived
@@ -80,6 +81,13 @@ def _load():
                 ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                 ctypes.c_int, ctypes.c_int, ctypes.c_double,
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+            lib.gna_oracle_backward_kv_sel.restype = ctypes.c_int
+            lib.gna_oracle_backward_kv_sel.argtypes = [
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int,
+                ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
             lib.gna_oracle_window_starts.restype = None
             lib.gna_oracle_window_starts.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, ctypes.c_void_p]
@@ -194,3 +202,27 @@ def backward_dq_c(q, k, v, dout, dims, window, stride, sel, scale=None, rule=LEA
     if rc != 0:
         raise ValueError(f"gna_oracle_backward_dq_sel failed with {rc}")
     return dq
+
+
+def backward_kv_c(q, k, v, dout, dims, window, stride, sel, scale=None, rule=LEADER_CENTER, threads=None):
+    """dk and dv of the selected keys (flat ids, see :func:`query_ids`): two
+    float64 arrays ``[nsel, d]``.  Computes lse and delta for every query of the
+    planes that hold a selected key first (O(N |W| d) per plane)."""
+    q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float32) for x in (q, k, v, dout))
+    B, T, H, W, heads, d = q.shape
+    assert k.shape == q.shape and v.shape == q.shape and dout.shape == q.shape and (T, H, W) == tuple(dims)
+    if scale is None:
+        scale = default_scale(d)
+    if threads is None:
+        threads = os.cpu_count() or 1
+    sel = np.ascontiguousarray(sel, dtype=np.int64)
+    dk = np.empty((sel.size, d), dtype=np.float64)
+    dv = np.empty((sel.size, d), dtype=np.float64)
+    arr3 = ctypes.c_int * 3
+    rc = _load().gna_oracle_backward_kv_sel(
+        q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, B, heads,
+        arr3(*dims), arr3(*window), arr3(*stride), d, _rule_code(rule), float(scale),
+        sel.ctypes.data, sel.size, dk.ctypes.data, dv.ctypes.data, int(threads))
+    if rc != 0:
+        raise ValueError(f"gna_oracle_backward_kv_sel failed with {rc}")
+    return dk, dv

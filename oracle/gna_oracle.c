@@ -417,3 +417,184 @@ int gna_oracle_backward_dq_sel(const float *q, const float *k, const float *v, c
     free(th);
     return rc;
 }
+
+/*
+ * dk and dv of selected keys.  Phase 1 computes, for every query of each
+ * (b, head) plane that holds a selected key, lse_i and delta_i = sum_l p_il
+ * <dout_i, v_l>.  Phase 2 walks, per selected key j, the queries whose window
+ * holds j (per dimension an interval of positions, found by scanning the
+ * window starts) and sums their contributions:
+ *   dv_j = sum_i p_ij dout_i,   dk_j = scale sum_i p_ij (<dout_i, v_j> - delta_i) q_i.
+ * sel: flat key ids ((b*heads + h)*N + (t*H + y)*W + x); dk, dv: double [nsel, d].
+ */
+typedef struct {
+    const bjob_t *J;
+    const int *planes;       /* planes needing lse / delta */
+    int nplanes;
+    int64_t begin, end;      /* range over nplanes * N queries */
+    double *lse, *delta;     /* [B*heads*N], only the listed planes filled */
+    const int64_t *sel;      /* phase 2 */
+    int64_t kbegin, kend;
+    double *dk, *dv;
+    int status;
+} kvjob_t;
+
+static void *kv_phase1(void *arg)
+{
+    kvjob_t *Q = (kvjob_t *)arg;
+    const bjob_t *J = Q->J;
+    const int T = J->dims[0], H = J->dims[1], W = J->dims[2], d = J->d;
+    const int64_t N = (int64_t)T * H * W;
+    int64_t wsz = (int64_t)J->win[0] * J->win[1] * J->win[2];
+    double *pbuf = (double *)malloc(sizeof(double) * (size_t)wsz);
+    double *dpbuf = (double *)malloc(sizeof(double) * (size_t)wsz);
+    if (!pbuf || !dpbuf) { free(pbuf); free(dpbuf); Q->status = -2; return NULL; }
+    for (int64_t r = Q->begin; r < Q->end; ++r) {
+        const int plane = Q->planes[r / N];
+        const int64_t tok = r % N;
+        const int h = plane % J->heads, b = plane / J->heads;
+        const int x = (int)(tok % W), y = (int)((tok / W) % H), t = (int)(tok / ((int64_t)W * H));
+        const int a0 = start_of(t, T, J->win[0], J->str[0], J->rule);
+        const int a1 = start_of(y, H, J->win[1], J->str[1], J->rule);
+        const int a2 = start_of(x, W, J->win[2], J->str[2], J->rule);
+        const int64_t qi = row_of(J, b, t, y, x, h) * d;
+        int64_t n = 0;
+        double m = -INFINITY;
+        for (int kt = a0; kt < a0 + J->win[0]; ++kt)
+            for (int ky = a1; ky < a1 + J->win[1]; ++ky)
+                for (int kx = a2; kx < a2 + J->win[2]; ++kx) {
+                    const int64_t kj = row_of(J, b, kt, ky, kx, h) * d;
+                    double acc = 0.0, dacc = 0.0;
+                    for (int c = 0; c < d; ++c) {
+                        acc += (double)J->q[qi + c] * (double)J->k[kj + c];
+                        dacc += (double)J->dout[qi + c] * (double)J->v[kj + c];
+                    }
+                    pbuf[n] = J->scale * acc;
+                    dpbuf[n] = dacc;
+                    if (pbuf[n] > m) m = pbuf[n];
+                    ++n;
+                }
+        double z = 0.0, dsum = 0.0;
+        for (int64_t l = 0; l < n; ++l) { pbuf[l] = exp(pbuf[l] - m); z += pbuf[l]; }
+        for (int64_t l = 0; l < n; ++l) dsum += pbuf[l] / z * dpbuf[l];
+        const int64_t flat = (int64_t)plane * N + tok;
+        Q->lse[flat] = m + log(z);
+        Q->delta[flat] = dsum;
+    }
+    free(pbuf);
+    free(dpbuf);
+    return NULL;
+}
+
+/* query positions of one dimension whose window holds key position j: [lo, hi] */
+static void inverse_window(int j, int L, int w, int s, int rule, int *lo, int *hi)
+{
+    *lo = 1;
+    *hi = 0;
+    for (int i = 0; i < L; ++i) {
+        const int a = start_of(i, L, w, s, rule);
+        if (a <= j && j < a + w) {
+            if (*lo > *hi) *lo = i;
+            *hi = i;
+        }
+    }
+}
+
+static void *kv_phase2(void *arg)
+{
+    kvjob_t *Q = (kvjob_t *)arg;
+    const bjob_t *J = Q->J;
+    const int T = J->dims[0], H = J->dims[1], W = J->dims[2], d = J->d;
+    const int64_t N = (int64_t)T * H * W;
+    for (int64_t r = Q->kbegin; r < Q->kend; ++r) {
+        const int64_t flat = Q->sel[r];
+        const int64_t tok = flat % N, plane = flat / N;
+        const int h = (int)(plane % J->heads), b = (int)(plane / J->heads);
+        const int x = (int)(tok % W), y = (int)((tok / W) % H), t = (int)(tok / ((int64_t)W * H));
+        const int64_t kj = row_of(J, b, t, y, x, h) * d;
+        int lo[3], hi[3];
+        inverse_window(t, T, J->win[0], J->str[0], J->rule, &lo[0], &hi[0]);
+        inverse_window(y, H, J->win[1], J->str[1], J->rule, &lo[1], &hi[1]);
+        inverse_window(x, W, J->win[2], J->str[2], J->rule, &lo[2], &hi[2]);
+        double *dk = Q->dk + r * d, *dv = Q->dv + r * d;
+        for (int c = 0; c < d; ++c) { dk[c] = 0.0; dv[c] = 0.0; }
+        for (int qt = lo[0]; qt <= hi[0]; ++qt)
+            for (int qy = lo[1]; qy <= hi[1]; ++qy)
+                for (int qx = lo[2]; qx <= hi[2]; ++qx) {
+                    const int64_t qi = row_of(J, b, qt, qy, qx, h) * d;
+                    const int64_t qflat = plane * N + ((int64_t)qt * H + qy) * W + qx;
+                    double acc = 0.0, dacc = 0.0;
+                    for (int c = 0; c < d; ++c) {
+                        acc += (double)J->q[qi + c] * (double)J->k[kj + c];
+                        dacc += (double)J->dout[qi + c] * (double)J->v[kj + c];
+                    }
+                    const double p = exp(J->scale * acc - Q->lse[qflat]);
+                    const double ds = p * (dacc - Q->delta[qflat]);
+                    for (int c = 0; c < d; ++c) {
+                        dv[c] += p * (double)J->dout[qi + c];
+                        dk[c] += J->scale * ds * (double)J->q[qi + c];
+                    }
+                }
+    }
+    return NULL;
+}
+
+static int run_kv_jobs(kvjob_t *jobs, int n, void *(*fn)(void *))
+{
+    pthread_t *th = (pthread_t *)calloc((size_t)n, sizeof(pthread_t));
+    if (!th) return -2;
+    if (n == 1) {
+        fn(&jobs[0]);
+    } else {
+        for (int i = 0; i < n; ++i) pthread_create(&th[i], NULL, fn, &jobs[i]);
+        for (int i = 0; i < n; ++i) pthread_join(th[i], NULL);
+    }
+    free(th);
+    int rc = 0;
+    for (int i = 0; i < n; ++i) if (jobs[i].status) rc = jobs[i].status;
+    return rc;
+}
+
+int gna_oracle_backward_kv_sel(const float *q, const float *k, const float *v, const float *dout,
+                               int B, int heads, const int dims[3], const int window[3],
+                               const int stride[3], int head_dim, int rule, double scale,
+                               const int64_t *sel, int64_t nsel, double *dk, double *dv, int nthreads)
+{
+    if (B < 1 || heads < 1 || head_dim < 1 || (rule != 0 && rule != 1) || !sel || nsel < 0) return -1;
+    for (int i = 0; i < 3; ++i)
+        if (!(1 <= stride[i] && stride[i] <= window[i] && window[i] <= dims[i])) return -1;
+    const int64_t N = (int64_t)dims[0] * dims[1] * dims[2];
+    const int planes_all = B * heads;
+    for (int64_t r = 0; r < nsel; ++r)
+        if (sel[r] < 0 || sel[r] >= (int64_t)planes_all * N) return -1;
+    bjob_t J;
+    memset(&J, 0, sizeof(J));
+    J.q = q; J.k = k; J.v = v; J.dout = dout;
+    J.B = B; J.heads = heads; J.d = head_dim; J.rule = rule; J.scale = scale;
+    for (int c = 0; c < 3; ++c) { J.dims[c] = dims[c]; J.win[c] = window[c]; J.str[c] = stride[c]; }
+    /* planes holding a selected key */
+    char *need = (char *)calloc((size_t)planes_all, 1);
+    int *planes = (int *)calloc((size_t)planes_all, sizeof(int));
+    double *lse = (double *)calloc((size_t)(planes_all * N), sizeof(double));
+    double *delta = (double *)calloc((size_t)(planes_all * N), sizeof(double));
+    if (nthreads < 1) nthreads = 1;
+    kvjob_t *jobs = (kvjob_t *)calloc((size_t)nthreads, sizeof(kvjob_t));
+    int rc = 0;
+    if (!need || !planes || !lse || !delta || !jobs) { rc = -2; goto done; }
+    int nplanes = 0;
+    for (int64_t r = 0; r < nsel; ++r) need[sel[r] / N] = 1;
+    for (int p = 0; p < planes_all; ++p) if (need[p]) planes[nplanes++] = p;
+    const int64_t nq = (int64_t)nplanes * N;
+    for (int i = 0; i < nthreads; ++i) {
+        jobs[i].J = &J; jobs[i].planes = planes; jobs[i].nplanes = nplanes;
+        jobs[i].begin = nq * i / nthreads; jobs[i].end = nq * (i + 1) / nthreads;
+        jobs[i].lse = lse; jobs[i].delta = delta;
+        jobs[i].sel = sel; jobs[i].kbegin = nsel * i / nthreads; jobs[i].kend = nsel * (i + 1) / nthreads;
+        jobs[i].dk = dk; jobs[i].dv = dv;
+    }
+    rc = run_kv_jobs(jobs, nthreads, kv_phase1);
+    if (rc == 0) rc = run_kv_jobs(jobs, nthreads, kv_phase2);
+done:
+    free(need); free(planes); free(lse); free(delta); free(jobs);
+    return rc;
+}

@@ -8,7 +8,7 @@
 * stride = window on a divisible grid: the same, block by block;
 * window 1: out = v exactly, so dv = dout and dq = dk = 0;
 * the C and the loop versions agree on random cases, and the selected-query dq
-  of the C oracle equals its whole-plane dq;
+  and selected-key dk, dv of the C oracle equal its whole-plane results;
 * three identities of the derivative that hold at any size (sums of dv and dk,
   and sum <dq, q> = sum <dk, k>);
 * planted mistakes in the softmax Jacobian are caught by the finite differences.
@@ -148,6 +148,22 @@ def test_selected_query_dq_matches_whole_planes():
     ids = oracle.query_ids(sel[:, 0], sel[:, 1], sel[:, 2], sel[:, 3], sel[:, 4], 3, dims)
     got = oracle.backward_dq_c(q, k, v, dout, dims, window, stride, ids, threads=3)
     np.testing.assert_allclose(got, dq[sel[:, 0], sel[:, 2], sel[:, 3], sel[:, 4], sel[:, 1]], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("dims,window,stride,rule", [
+    ((3, 6, 7), (2, 3, 5), (1, 2, 3), ref.LEADER_CENTER),
+    ((2, 8, 9), (2, 4, 4), (2, 4, 4), ref.LEADER_LITERAL),
+])
+def test_selected_key_dk_dv_match_whole_planes(dims, window, stride, rule):
+    q, k, v, dout = (x.astype(np.float32) for x in _inputs(28, 2, dims, 3, 8))
+    _, dk, dv = oracle.backward_c(q, k, v, dout, dims, window, stride, rule=rule, threads=2)
+    rng = np.random.default_rng(28)
+    sel = np.array([tuple(int(rng.integers(0, n)) for n in (2, 3) + dims) for _ in range(40)])
+    ids = oracle.query_ids(sel[:, 0], sel[:, 1], sel[:, 2], sel[:, 3], sel[:, 4], 3, dims)
+    gk, gv = oracle.backward_kv_c(q, k, v, dout, dims, window, stride, ids, rule=rule, threads=3)
+    at = (sel[:, 0], sel[:, 2], sel[:, 3], sel[:, 4], sel[:, 1])
+    np.testing.assert_allclose(gk, dk[at], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(gv, dv[at], rtol=0, atol=1e-12)
 
 
 def _jac_no_centering(p, dp):
