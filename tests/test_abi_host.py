@@ -295,3 +295,22 @@ def test_schedule_step_rejects_bad_steps(args):
         G.gna_schedule_step(*args, (1, 16, 16), (1, 5, 5), (1, 1, 1))
     with pytest.raises(G.GNAError):
         G.gna_schedule_step(0, 28, 9, (1, 16, 16), (1, 17, 5), (1, 1, 1))
+
+
+def test_backward_binding_checks_tensor_sizes():
+    import torch
+    B, heads, dims, d = 1, 1, (1, 16, 16), 128
+    nt = G.gna_tiled_elems(B, heads, dims, d)
+    bf = torch.bfloat16
+    ok, small = torch.empty(nt, dtype=bf), torch.empty(nt - 1, dtype=bf)
+    rows, rows_small = torch.empty(nt // d, dtype=torch.float32), torch.empty(nt // d - 1, dtype=torch.float32)
+    with pytest.raises(ValueError, match="delta holds"):
+        G.gna_backward_delta(ok, ok, rows_small, B, heads, dims, d)
+    with pytest.raises(ValueError, match="dq holds"):
+        G.gna_backward_dq(ok, ok, ok, ok, ok, rows, rows, small, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
+    with pytest.raises(ValueError, match="lse holds"):
+        G.gna_backward_dkdv(ok, ok, ok, ok, rows_small, rows, ok, ok, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
+    with pytest.raises(ValueError, match="dv holds"):
+        G.gna_backward_dkdv(ok, ok, ok, ok, rows, rows, ok, small, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
+    with pytest.raises(ValueError, match="bfloat16"):
+        G.gna_backward_dq(ok.float(), ok, ok, ok, ok, rows, rows, ok, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
