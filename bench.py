@@ -38,6 +38,7 @@ import torch  # noqa: E402
 METRIC = "GNA fwd useful TFLOP/s on 1 B300 and % of dense tensor peak; speedup vs dense attn"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gna_fwd_traffic.json")
+E4M3_PEAK_FILE = os.path.join(ROOT, "profiles", "e4m3_gemm_peak.json")
 FWD_SOURCE = os.path.join(ROOT, "dimensional_sparse_attention_gna_b300", "csrc", "gna_fwd.cu")
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
@@ -64,6 +65,9 @@ def parse_args(argv=None):
                     help="also run the forward back to back for this many seconds and report the sustained rate")
     ap.add_argument("--backward", action="store_true",
                     help="also time the backward pass (delta, dq, dk/dv kernels; bf16, head_dim 128, tiled layout)")
+    ap.add_argument("--measure-e4m3-gemm", action="store_true",
+                    help="only time a dense e4m3 GEMM (torch._scaled_mm, 8192^3, bf16 out) as a burst and "
+                         "for 4 s back to back, print one JSON line and exit")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0,
@@ -86,12 +90,75 @@ def workload_name(a) -> str:
             f"window {'x'.join(map(str, a.window))}, stride {'x'.join(map(str, a.stride))}, B={a.batch}, {a.dtype}")
 
 
+def run_config(a, world: int = 1) -> dict:
+    """The ``config`` object of both arms' JSON lines (identical keys)."""
+    esz = 2 if a.dtype == "bf16" else 1
+    return {"workload": workload_name(a), "dims": list(a.dims), "window": list(a.window),
+            "stride": list(a.stride), "heads": a.heads, "B": a.batch, "head_dim": a.head_dim,
+            "layout": a.layout,
+            "l2": "inputs larger than L2 (3 x %.0f MB raster + tiled copies)" % (
+                a.batch * math.prod(a.dims) * a.heads * a.head_dim * esz / 1e6),
+            "parallelism": f"replicas x{world}: every rank runs the full workload on its own data"}
+
+
 def load_peaks():
     try:
         with open(PEAKS_FILE) as f:
             return json.load(f), "measured"
     except OSError:
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_e4m3_peak():
+    """The dense e4m3 GEMM rate measured on the B300s by ``--measure-e4m3-gemm``
+    (recorded in profiles/), or None."""
+    try:
+        with open(E4M3_PEAK_FILE) as f:
+            rec = json.load(f)
+        return float(rec["e4m3_tflops"]), float(rec["e4m3_tflops_sustained"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measure_e4m3_gemm(n: int = 8192, seconds: float = 4.0) -> dict:
+    """Dense e4m3 x e4m3 -> bf16 GEMM through torch._scaled_mm (cuBLASLt): the
+    fp8 counterpart of the driver's bf16 cuBLAS figures (2 n^3 flops per GEMM;
+    best of 10 as the burst rate, then back to back for `seconds`)."""
+    dev = torch.device("cuda")
+    a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+    b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()      # column-major operand
+    one = torch.ones((), device=dev)
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps, t0 = 0, time.time()
+        e0.record()
+        while time.time() - t0 < seconds:
+            for _ in range(20):
+                mm()
+            reps += 20
+            torch.cuda.synchronize()
+        e1.record()
+        torch.cuda.synchronize()
+    flops = 2.0 * n ** 3
+    return {"e4m3_tflops": flops / (best / 1e3) / 1e12,
+            "e4m3_tflops_sustained": flops / (e0.elapsed_time(e1) / reps / 1e3) / 1e12,
+            "how": f"torch._scaled_mm e4m3 x e4m3 -> bf16, {n}^3 (2 n^3 flops): best of 10 (burst) and back "
+                   f"to back for {seconds:.0f} s (sustained), CUDA events",
+            "gpu_name": torch.cuda.get_device_name(), "clocks_sustained": clk.summary()}
 
 
 def kernel_traffic(a) -> int | None:
@@ -278,8 +345,7 @@ def reference_arm(a, rank, world):
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1000.0 * secs / a.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic: iid N(0,1) Q/K/V, rounded to the GPU input type",
-        "config": {"workload": workload_name(a), "dims": list(a.dims), "window": list(a.window),
-                   "stride": list(a.stride), "heads": a.heads, "B": a.batch, "head_dim": a.head_dim},
+        "config": run_config(a, world),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{nq} random queries of the workload over {a.steps} steps "
                                    "(plain C oracle, float64, one thread per core)"},
@@ -407,26 +473,41 @@ def gpu_arm(a, rank, world, local):
     mult = 2.0 if a.dtype == "fp8" else 1.0
     peak_burst = peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]) * mult
     peak_sustained = peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]) * mult
+    peak_source = f"{peaks_kind} {'bf16' if a.dtype == 'bf16' else 'fp8 (2x bf16)'} burst"
+    e4m3 = load_e4m3_peak() if a.dtype == "fp8" else None
+    if e4m3 is not None:
+        # the e4m3 GEMM rate measured on the same pool replaces the 2x bf16 ratio
+        peak_burst, peak_sustained = e4m3
+        peak_source = "measured e4m3 cuBLASLt GEMM burst (profiles/e4m3_gemm_peak.json)"
 
     # tile-level work of the launch (what the tensor cores execute)
     visited, partial, nq = G.gna_tile_stats(dims, a.window, a.stride)
     tile_flops = 4.0 * B * heads * visited * 128 * 128 * d
 
     # dense attention through the same kernel on the same tokens (window = grid)
+    # (same warm-up and step count as the GNA launches, clocks sampled alike, so
+    # that the speedup can also be compared at equal clock: time x median MHz)
     speedup = None
     dense_ms = None
+    dense_clk = None
+    speedup_clock_normalised = None
     if not a.no_dense:
-        forward(dims, (1, 1, 1), xs[0], xs[1], out, lse)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 2
-        e0.record(stream)
-        for _ in range(reps):
+        for _ in range(a.warmup):
             forward(dims, (1, 1, 1), xs[0], xs[1], out, lse)
-        e1.record(stream)
         torch.cuda.synchronize()
+        dense_ev = []
+        with ClockSampler(gpu_index) as dclocks:
+            for _ in range(a.steps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                forward(dims, (1, 1, 1), xs[0], xs[1], out, lse)
+                e1.record(stream)
+                dense_ev.append((e0, e1))
+            torch.cuda.synchronize()
         G.gna_get_status(stream)
-        dense_ms = e0.elapsed_time(e1) / reps
+        dense_ms = statistics.mean(e0.elapsed_time(e1) for e0, e1 in dense_ev)
         speedup = dense_ms / fwd_ms
+        dense_clk = dclocks.summary()
 
     # end to end through the public API with host buffers: every step copies its
     # Q, K, V from pinned host memory, runs the step's kernels and copies O and
@@ -475,7 +556,7 @@ def gpu_arm(a, rank, world, local):
         torch.cuda.synchronize()
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e2e_steps = max(4, min(a.steps, 8))
+        e2e_steps = a.steps
         e0.record(s_in)
         for k in range(e2e_steps):
             e2e_step(k)
@@ -493,6 +574,9 @@ def gpu_arm(a, rank, world, local):
                "pipelining": "uploads, kernels and downloads of consecutive steps on three streams"}
 
     clk = clocks.summary()
+    if speedup is not None and clk and dense_clk and clk.get("sm_mhz") and dense_clk.get("sm_mhz"):
+        # cycles instead of seconds: each arm's time x its median SM clock
+        speedup_clock_normalised = (dense_ms * dense_clk["sm_mhz"]) / (fwd_ms * clk["sm_mhz"])
 
     # optional: the forward launched back to back for several seconds, long
     # enough for the board to reach its average power cap
@@ -576,15 +660,10 @@ def gpu_arm(a, rank, world, local):
         "warmup": a.warmup, "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": a.dtype,
         "data": "synthetic: iid N(0,1) Q/K/V drawn on the device per rank",
-        "config": {"workload": workload_name(a), "dims": list(dims), "window": list(a.window),
-                   "stride": list(a.stride), "heads": heads, "B": B, "head_dim": d,
-                   "tile": list(G.gna_tile_shape(dims)), "layout": a.layout,
-                   "l2": "inputs larger than L2 (3 x %.0f MB raster + tiled copies)" % (
-                       B * math.prod(dims) * heads * d * esz / 1e6),
-                   "parallelism": f"replicas x{world}: every rank runs the full workload on its own data"},
+        "config": run_config(a, world), "tile": list(G.gna_tile_shape(dims)),
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": kernel_tflops / peak_burst, "traffic": traffic,
-                     "peak_source": f"{peaks_kind} {'bf16' if a.dtype == 'bf16' else 'fp8 (2x bf16)'} burst",
+                     "peak_source": peak_source,
                      "frac_of_sustained_peak": kernel_tflops / peak_sustained,
                      "tile_work_tflops": tile_flops / (fwd_ms / 1e3) / 1e12,
                      "tile_overhead": tile_flops / flops_rank, "partial_tile_share": partial / visited},
@@ -594,6 +673,7 @@ def gpu_arm(a, rank, world, local):
         "permute_frac_of_hbm": perm_bytes / (perm_ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6400.0),
         "unpermute_gbps": None if raster else unperm_bytes / (unperm_ms / 1e3) / 1e9,
         "dense_forward_ms": dense_ms, "speedup_vs_dense": speedup,
+        "dense_clocks": dense_clk, "speedup_vs_dense_clock_normalised": speedup_clock_normalised,
         "flop_sparsity_ratio": n_ratio,
         "speedup_bound_at_equal_tile_rate": G.gna_plan_tile(dims, a.window, a.stride)[2],
         "speedup_over_ratio": None if speedup is None else speedup / n_ratio,
@@ -605,6 +685,9 @@ def gpu_arm(a, rank, world, local):
 
 def main(argv=None):
     a = parse_args(argv)
+    if a.measure_e4m3_gemm:
+        print(json.dumps(measure_e4m3_gemm()), flush=True)
+        return
     rank, world, local = dist_setup(a)
     try:
         if a.impl == "reference":

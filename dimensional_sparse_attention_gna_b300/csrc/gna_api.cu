@@ -1,6 +1,7 @@
 // C ABI of libgna_b300.so (declared in include/gna.h): argument validation,
 // tile planning, TMA descriptor encoding and kernel launches.  Nothing here
 // allocates device memory; every call enqueues on the caller's stream.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -21,6 +22,11 @@
 namespace {
 
 thread_local std::string t_last_error;
+
+// Failure injection of the bounded-wait tests (gna_test_skip_kv_load): the KV
+// load iteration the producer of the forward / dQ kernel skips, -1 = none.
+std::atomic<int> g_skip_kv_forward{-1};
+std::atomic<int> g_skip_kv_backward_dq{-1};
 
 gna_status fail(gna_status s, const char* fmt, ...)
 {
@@ -296,6 +302,12 @@ int64_t gna_tiled_elems(int B, int heads, const int dims[3], const int tile_in[3
     return n;
 }
 
+size_t gna_permuted_elems(int B, int heads, const int dims[3], int head_dim)
+{
+    const int64_t n = gna_tiled_elems(B, heads, dims, nullptr, head_dim);
+    return n < 0 ? 0 : static_cast<size_t>(n);
+}
+
 gna_status gna_permute(const void* src, void* dst, int B, int heads, const int dims[3], int head_dim,
                        gna_dtype dtype, void* stream)
 {
@@ -450,6 +462,9 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
     if (opt && !(opt->scale >= 0.0f && std::isfinite(opt->scale)))
         return fail(GNA_ERR_INVALID_ARG, "scale must be finite and >= 0");
     if (opt && opt->descale && es != 1) return fail(GNA_ERR_INVALID_ARG, "descale is only used with GNA_FP8_E4M3");
+    if (es == 1 && (opt == nullptr || opt->descale == nullptr))
+        return fail(GNA_ERR_INVALID_ARG, "GNA_FP8_E4M3 needs the per-tensor descales of q, k, v "
+                                         "(gna_forward_fp8, or gna_options.descale)");
     if (opt && opt->descale && (reinterpret_cast<uintptr_t>(opt->descale) & 3u))
         return fail(GNA_ERR_INVALID_ARG, "descale must be 4-byte aligned");
 
@@ -476,8 +491,7 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
     p.lse = lse;
     p.descale = (opt && es == 1) ? opt->descale : nullptr;
     p.scale = (opt && opt->scale > 0.0f) ? opt->scale : 1.0f / std::sqrt(static_cast<float>(head_dim));
-    p.fault_skip_kv = -1;
-    if (const char* f = std::getenv("GNA_TEST_SKIP_KV_LOAD")) p.fault_skip_kv = std::atoi(f);
+    p.fault_skip_kv = g_skip_kv_forward.load(std::memory_order_relaxed);
 
     p.q = q;
     p.raster = raster ? 1 : 0;
@@ -510,7 +524,21 @@ gna_status gna_forward(const void* q, const void* k, const void* v, void* out, f
                        const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
                        void* stream)
 {
+    if (dtype == GNA_FP8_E4M3)
+        return fail(GNA_ERR_INVALID_ARG, "gna_forward takes GNA_BF16; e4m3 codes need their descales: "
+                                         "call gna_forward_fp8");
     return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, nullptr, stream, false);
+}
+
+gna_status gna_forward_fp8(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
+                           const int dims[3], const int window[3], const int stride[3], int head_dim,
+                           const float* descale_qkv, void* stream)
+{
+    if (descale_qkv == nullptr) return fail(GNA_ERR_INVALID_ARG, "descale_qkv is NULL");
+    gna_options opt{};
+    opt.descale = descale_qkv;
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, GNA_FP8_E4M3, &opt, stream,
+                        false);
 }
 
 gna_status gna_forward_raster(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
@@ -534,6 +562,16 @@ gna_status gna_schedule_step(int step, int num_steps, int full_steps, const int 
         out_window[d] = full ? dims[d] : window[d];
         out_stride[d] = full ? 1 : stride[d];
     }
+    t_last_error.clear();
+    return GNA_OK;
+}
+
+gna_status gna_test_skip_kv_load(int kernel, int kv_index)
+{
+    const int v = kv_index < 0 ? -1 : kv_index;
+    if (kernel == 0) g_skip_kv_forward.store(v, std::memory_order_relaxed);
+    else if (kernel == 1) g_skip_kv_backward_dq.store(v, std::memory_order_relaxed);
+    else return fail(GNA_ERR_INVALID_ARG, "unknown kernel %d (0 = forward, 1 = dQ backward)", kernel);
     t_last_error.clear();
     return GNA_OK;
 }
@@ -674,8 +712,7 @@ gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, co
     p.lse = lse;
     p.delta = delta;
     p.dq = dq;
-    p.fault_skip_kv = -1;
-    if (const char* f = std::getenv("GNA_TEST_SKIP_BWD_LOAD")) p.fault_skip_kv = std::atoi(f);
+    p.fault_skip_kv = g_skip_kv_backward_dq.load(std::memory_order_relaxed);
     const int64_t rows = nq * gna::kTileElems;
     if ((st = make_tile_map(&p.tmK, k, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_tile_map(&p.tmV, v, rows, head_dim, 2)) != GNA_OK) return st;

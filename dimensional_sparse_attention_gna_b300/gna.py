@@ -93,6 +93,12 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(GNAOptions), _P]
         L.gna_forward_raster.restype = st
         L.gna_forward_raster.argtypes = L.gna_forward_ex.argtypes
+        L.gna_forward_fp8.restype = st
+        L.gna_forward_fp8.argtypes = [_P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _P, _P]
+        L.gna_permuted_elems.restype = ctypes.c_size_t
+        L.gna_permuted_elems.argtypes = [_INT, _INT, _I3, _INT]
+        L.gna_test_skip_kv_load.restype = st
+        L.gna_test_skip_kv_load.argtypes = [_INT, _INT]
         L.gna_backward_delta.restype = st
         L.gna_backward_delta.argtypes = [_P, _P, _P, _INT, _INT, _I3, _INT, _INT, ctypes.POINTER(GNAOptions), _P]
         L.gna_backward_dq.restype = st
@@ -120,10 +126,22 @@ def _check(status: int):
         raise GNAError(status, lib().gna_last_error().decode())
 
 
-def _stream_ptr(stream) -> int | None:
+def _stream_ptr(stream, device: torch.device | None = None) -> int | None:
+    """The stream handle a call enqueues on.  ``device`` is the device of the
+    call's tensors: the C ABI works on the current CUDA device (its TMA
+    descriptors and launches assume it), so tensors elsewhere are refused."""
+    if device is not None and device.type != "cuda":
+        raise ValueError("tensors must live on a CUDA device")
+    if device is not None:
+        cur = torch.cuda.current_device()
+        if device.index is not None and device.index != cur:
+            raise ValueError(f"tensors live on {device}, but the current CUDA device is cuda:{cur}; "
+                             "call under torch.cuda.device(...)")
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, torch.cuda.Stream):
+        if device is not None and stream.device != device:
+            raise ValueError(f"stream of {stream.device} for tensors on {device}")
         return stream.cuda_stream
     return int(stream)
 
@@ -142,9 +160,10 @@ def _raster_elems(B: int, heads: int, dims, head_dim: int) -> int:
     return B * dims[0] * dims[1] * dims[2] * heads * head_dim
 
 
-def _need(**tensors_and_sizes):
+def _need(**tensors_and_sizes) -> torch.device | None:
     """Every tensor must hold at least the elements the call touches (the C ABI
-    takes bare pointers and cannot check), and all must share one device."""
+    takes bare pointers and cannot check), and all must share one device, which
+    is returned."""
     devices = set()
     for name, (t, n) in tensors_and_sizes.items():
         if t is None:
@@ -154,6 +173,7 @@ def _need(**tensors_and_sizes):
         devices.add(t.device)
     if len(devices) > 1:
         raise ValueError(f"tensors on different devices: {sorted(map(str, devices))}")
+    return next(iter(devices)) if devices else None
 
 
 def dtype_code(dtype: torch.dtype) -> int:
@@ -193,13 +213,14 @@ def gna_permute(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims, 
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
-    _need(src=(src, _raster_elems(B, heads, dims, head_dim)),
-          dst=(dst, gna_tiled_elems(B, heads, dims, head_dim, tile)))
+    dev = _need(src=(src, _raster_elems(B, heads, dims, head_dim)),
+                dst=(dst, gna_tiled_elems(B, heads, dims, head_dim, tile)))
+    stream = _stream_ptr(stream, dev)
     if tile is None:
-        st = lib().gna_permute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+        st = lib().gna_permute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, stream)
     else:
         st = lib().gna_permute_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
-                                     _stream_ptr(stream))
+                                     stream)
     _check(st)
 
 
@@ -209,13 +230,14 @@ def gna_unpermute(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
-    _need(src=(src, gna_tiled_elems(B, heads, dims, head_dim, tile)),
-          dst=(dst, _raster_elems(B, heads, dims, head_dim)))
+    dev = _need(src=(src, gna_tiled_elems(B, heads, dims, head_dim, tile)),
+                dst=(dst, _raster_elems(B, heads, dims, head_dim)))
+    stream = _stream_ptr(stream, dev)
     if tile is None:
-        st = lib().gna_unpermute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+        st = lib().gna_unpermute(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, stream)
     else:
         st = lib().gna_unpermute_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
-                                       _stream_ptr(stream))
+                                       stream)
     _check(st)
 
 
@@ -231,13 +253,14 @@ def gna_permute_v(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, dims
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
-    _need(src=(src, _raster_elems(B, heads, dims, head_dim)),
-          dst=(dst, gna_tiled_elems(B, heads, dims, head_dim, tile)))
+    dev = _need(src=(src, _raster_elems(B, heads, dims, head_dim)),
+                dst=(dst, gna_tiled_elems(B, heads, dims, head_dim, tile)))
+    stream = _stream_ptr(stream, dev)
     if tile is None:
-        st = lib().gna_permute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+        st = lib().gna_permute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, stream)
     else:
         st = lib().gna_permute_v_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
-                                       _stream_ptr(stream))
+                                       stream)
     _check(st)
 
 
@@ -247,86 +270,109 @@ def gna_unpermute_v(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, di
     code = dtype_code(src.dtype)
     if dst.dtype != src.dtype:
         raise ValueError("src and dst dtypes differ")
-    _need(src=(src, gna_tiled_elems(B, heads, dims, head_dim, tile)),
-          dst=(dst, _raster_elems(B, heads, dims, head_dim)))
+    dev = _need(src=(src, gna_tiled_elems(B, heads, dims, head_dim, tile)),
+                dst=(dst, _raster_elems(B, heads, dims, head_dim)))
+    stream = _stream_ptr(stream, dev)
     if tile is None:
-        st = lib().gna_unpermute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, _stream_ptr(stream))
+        st = lib().gna_unpermute_v(_ptr(src), _ptr(dst), B, heads, _I3(*dims), head_dim, code, stream)
     else:
         st = lib().gna_unpermute_v_tiled(_ptr(src), _ptr(dst), B, heads, _I3(*dims), _I3(*tile), head_dim, code,
-                                         _stream_ptr(stream))
+                                         stream)
     _check(st)
 
 
-def gna_forward(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor | None,
-                B: int, heads: int, dims, window, stride, head_dim: int, *, tile=None,
+def _descale_arg(descale: torch.Tensor | None) -> torch.Tensor | None:
+    if descale is not None and (descale.dtype != torch.float32 or descale.numel() != 3):
+        raise ValueError("descale must be 3 float32 values")
+    return descale
+
+
+def gna_forward(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out: torch.Tensor,
+                lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int, *, tile=None,
                 leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, descale: torch.Tensor | None = None,
                 stream=None):
     """GNA forward on tiled tensors (see ``include/gna.h``).
 
-    ``q, k``: bf16 or float8_e4m3fn, tiled; ``v``: same dtype, value layout
-    (:func:`gna_permute_v`); ``out``: bf16 tiled; ``lse``:
-    float32 ``[B, heads, tiles, 128]`` or None; ``descale``: float32 device
-    tensor of 3 values (e4m3 only) or None.
+    ``q, k``: bf16 or float8_e4m3fn, tiled; ``v_value``: same dtype, V in the
+    VALUE layout (:func:`gna_permute_v`, not :func:`gna_permute`); ``out``:
+    bf16 tiled; ``lse``: float32 ``[B, heads, tiles, 128]`` or None;
+    ``descale``: float32 device tensor of 3 values, required for e4m3 and
+    refused for bf16.  The plain bf16 call goes to ``gna_forward``, an e4m3
+    call with default options to ``gna_forward_fp8``, anything else to
+    ``gna_forward_ex``.
     """
     code = dtype_code(q.dtype)
-    if k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must share a dtype")
+    if k.dtype != q.dtype or v_value.dtype != q.dtype:
+        raise ValueError("q, k, v_value must share a dtype")
     if out.dtype != torch.bfloat16:
         raise ValueError("out must be bfloat16")
     if lse is not None and lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
+    descale = _descale_arg(descale)
     nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
-    _need(q=(q, nt), k=(k, nt), v=(v, nt), out=(out, nt), lse=(lse, nt // head_dim))
-    plain = tile is None and leader_rule == GNA_LEADER_CENTER and scale == 0.0 and descale is None
-    if plain:
-        st = lib().gna_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
-                               _I3(*window), _I3(*stride), head_dim, code, _stream_ptr(stream))
+    dev = _need(q=(q, nt), k=(k, nt), v_value=(v_value, nt), out=(out, nt), lse=(lse, nt // head_dim),
+                descale=(descale, 3))
+    st_ptr = _stream_ptr(stream, dev)
+    defaults = tile is None and leader_rule == GNA_LEADER_CENTER and scale == 0.0
+    if defaults and code == GNA_BF16 and descale is None:
+        st = lib().gna_forward(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+                               _I3(*window), _I3(*stride), head_dim, code, st_ptr)
+    elif defaults and code == GNA_FP8_E4M3 and descale is not None:
+        st = lib().gna_forward_fp8(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+                                   _I3(*window), _I3(*stride), head_dim, _ptr(descale), st_ptr)
     else:
         opt = GNAOptions()
         opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
         opt.leader_rule = leader_rule
         opt.scale = scale
-        if descale is not None:
-            if descale.dtype != torch.float32 or descale.numel() != 3:
-                raise ValueError("descale must be 3 float32 values")
-            opt.descale = _ptr(descale)
-        st = lib().gna_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
-                                  _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
-                                  _stream_ptr(stream))
+        opt.descale = _ptr(descale)
+        st = lib().gna_forward_ex(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+                                  _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt), st_ptr)
     _check(st)
 
 
-def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+def gna_forward_fp8(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out: torch.Tensor,
+                    lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int,
+                    descale: torch.Tensor, *, stream=None):
+    """``gna_forward_fp8`` (see ``include/gna.h``): e4m3 codes, the 3 per-tensor
+    descales of q, k, v on the device, bf16 ``out``."""
+    if q.dtype != torch.float8_e4m3fn:
+        raise ValueError("gna_forward_fp8 takes float8_e4m3fn q, k, v_value")
+    if descale is None:
+        raise ValueError("descale is required")
+    gna_forward(q, k, v_value, out, lse, B, heads, dims, window, stride, head_dim, descale=descale, stream=stream)
+
+
+def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out: torch.Tensor,
                        lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int, *,
                        tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0,
                        descale: torch.Tensor | None = None, stream=None):
     """GNA forward with q, k, out and lse in the raster layout (see ``include/gna.h``).
 
-    ``q, k``: bf16 or float8_e4m3fn ``[B, T, H, W, heads, head_dim]``; ``v``:
-    same dtype, value layout (:func:`gna_permute_v` with the same ``tile``);
-    ``out``: bf16 raster; ``lse``: float32 ``[B, T, H, W, heads]`` or None.
+    ``q, k``: bf16 or float8_e4m3fn ``[B, T, H, W, heads, head_dim]``;
+    ``v_value``: same dtype, value layout (:func:`gna_permute_v` with the same
+    ``tile``); ``out``: bf16 raster; ``lse``: float32 ``[B, T, H, W, heads]``
+    or None; ``descale`` as for :func:`gna_forward`.
     """
     code = dtype_code(q.dtype)
-    if k.dtype != q.dtype or v.dtype != q.dtype:
-        raise ValueError("q, k, v must share a dtype")
+    if k.dtype != q.dtype or v_value.dtype != q.dtype:
+        raise ValueError("q, k, v_value must share a dtype")
     if out.dtype != torch.bfloat16:
         raise ValueError("out must be bfloat16")
     if lse is not None and lse.dtype != torch.float32:
         raise ValueError("lse must be float32")
+    descale = _descale_arg(descale)
     nr = _raster_elems(B, heads, dims, head_dim)
-    _need(q=(q, nr), k=(k, nr), v=(v, gna_tiled_elems(B, heads, dims, head_dim, tile)), out=(out, nr),
-          lse=(lse, nr // head_dim))
+    dev = _need(q=(q, nr), k=(k, nr), v_value=(v_value, gna_tiled_elems(B, heads, dims, head_dim, tile)),
+                out=(out, nr), lse=(lse, nr // head_dim), descale=(descale, 3))
     opt = GNAOptions()
     opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
     opt.leader_rule = leader_rule
     opt.scale = scale
-    if descale is not None:
-        if descale.dtype != torch.float32 or descale.numel() != 3:
-            raise ValueError("descale must be 3 float32 values")
-        opt.descale = _ptr(descale)
-    _check(lib().gna_forward_raster(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+    opt.descale = _ptr(descale)
+    _check(lib().gna_forward_raster(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                     _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
-                                    _stream_ptr(stream)))
+                                    _stream_ptr(stream, dev)))
 
 
 def gna_backward_delta(out: torch.Tensor, dout: torch.Tensor, delta: torch.Tensor, B: int, heads: int, dims,
@@ -335,11 +381,11 @@ def gna_backward_delta(out: torch.Tensor, dout: torch.Tensor, delta: torch.Tenso
     if out.dtype != torch.bfloat16 or dout.dtype != torch.bfloat16 or delta.dtype != torch.float32:
         raise ValueError("out, dout must be bfloat16 and delta float32")
     nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
-    _need(out=(out, nt), dout=(dout, nt), delta=(delta, nt // head_dim))
+    dev = _need(out=(out, nt), dout=(dout, nt), delta=(delta, nt // head_dim))
     opt = GNAOptions()
     opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
     _check(lib().gna_backward_delta(_ptr(out), _ptr(dout), _ptr(delta), B, heads, _I3(*dims), head_dim, GNA_BF16,
-                                    ctypes.byref(opt), _stream_ptr(stream)))
+                                    ctypes.byref(opt), _stream_ptr(stream, dev)))
 
 
 def gna_backward_dq(q: torch.Tensor, k: torch.Tensor, k_value: torch.Tensor, v: torch.Tensor, dout: torch.Tensor,
@@ -355,15 +401,15 @@ def gna_backward_dq(q: torch.Tensor, k: torch.Tensor, k_value: torch.Tensor, v: 
     if lse.dtype != torch.float32 or delta.dtype != torch.float32:
         raise ValueError("lse and delta must be float32")
     nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
-    _need(q=(q, nt), k=(k, nt), k_value=(k_value, nt), v=(v, nt), dout=(dout, nt), dq=(dq, nt),
-          lse=(lse, nt // head_dim), delta=(delta, nt // head_dim))
+    dev = _need(q=(q, nt), k=(k, nt), k_value=(k_value, nt), v=(v, nt), dout=(dout, nt), dq=(dq, nt),
+                lse=(lse, nt // head_dim), delta=(delta, nt // head_dim))
     opt = GNAOptions()
     opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
     opt.leader_rule = leader_rule
     opt.scale = scale
     _check(lib().gna_backward_dq(_ptr(q), _ptr(k), _ptr(k_value), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta),
                                  _ptr(dq), B, heads, _I3(*dims), _I3(*window), _I3(*stride), head_dim, GNA_BF16,
-                                 ctypes.byref(opt), _stream_ptr(stream)))
+                                 ctypes.byref(opt), _stream_ptr(stream, dev)))
 
 
 def gna_backward_dkdv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor,
@@ -378,15 +424,15 @@ def gna_backward_dkdv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: t
     if lse.dtype != torch.float32 or delta.dtype != torch.float32:
         raise ValueError("lse and delta must be float32")
     nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
-    _need(q=(q, nt), k=(k, nt), v=(v, nt), dout=(dout, nt), dk=(dk, nt), dv=(dv, nt), lse=(lse, nt // head_dim),
-          delta=(delta, nt // head_dim))
+    dev = _need(q=(q, nt), k=(k, nt), v=(v, nt), dout=(dout, nt), dk=(dk, nt), dv=(dv, nt),
+                lse=(lse, nt // head_dim), delta=(delta, nt // head_dim))
     opt = GNAOptions()
     opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
     opt.leader_rule = leader_rule
     opt.scale = scale
     _check(lib().gna_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dk),
                                    _ptr(dv), B, heads, _I3(*dims), _I3(*window), _I3(*stride), head_dim, GNA_BF16,
-                                   ctypes.byref(opt), _stream_ptr(stream)))
+                                   ctypes.byref(opt), _stream_ptr(stream, dev)))
 
 
 def gna_schedule_step(step: int, num_steps: int, full_steps: int, dims, window, stride):
@@ -414,6 +460,20 @@ def gna_plan_tile(dims, window, stride, leader_rule: int = GNA_LEADER_CENTER):
     _check(lib().gna_plan_tile(_I3(*dims), _I3(*window), _I3(*stride), leader_rule, t, ctypes.byref(ov),
                                ctypes.byref(sp)))
     return tuple(t), ov.value, sp.value
+
+
+def gna_permuted_elems(B: int, heads: int, dims, head_dim: int) -> int:
+    """Elements of one tensor written by :func:`gna_permute` under the default tile."""
+    n = lib().gna_permuted_elems(B, heads, _I3(*dims), head_dim)
+    if n == 0:
+        raise GNAError(GNA_ERR_INVALID_ARG, "invalid layout arguments")
+    return n
+
+
+def gna_test_skip_kv_load(kernel: int, kv_index: int):
+    """TEST ONLY (``gna_test_skip_kv_load``): kernel 0 = forward, 1 = dQ backward;
+    kv_index < 0 turns the injected skipped load off."""
+    _check(lib().gna_test_skip_kv_load(kernel, kv_index))
 
 
 def gna_get_status(stream=None):

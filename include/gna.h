@@ -58,7 +58,9 @@
  *   Launch failures return GNA_ERR_CUDA.  gna_last_error() gives a message.
  * * A kernel that gives up waiting on an internal pipeline barrier (a bound of
  *   about two seconds) records GNA_ERR_TIMEOUT in a device status word and
- *   exits cleanly; gna_get_status() reports it.
+ *   exits cleanly; its outputs are then incomplete although the call itself
+ *   returned GNA_OK.  Read gna_get_status() after the calls whose results
+ *   you use: it is the only report of such a failure.
  * * No C++ exception crosses this boundary.  Functions are thread-safe.
  */
 #ifndef GNA_B300_H
@@ -97,9 +99,10 @@ typedef struct {
     int tile[3];          /* layout tile; {0,0,0} = gna_tile_shape(dims)               */
     int leader_rule;      /* gna_leader_rule                                            */
     float scale;          /* softmax scale; 0 = 1/sqrt(head_dim)                        */
-    const float* descale; /* GNA_FP8_E4M3 only: device pointer to 3 floats, the
+    const float* descale; /* GNA_FP8_E4M3: device pointer to 3 floats, the
                              per-tensor dequantisation scales of q, k, v (value =
-                             code * descale); NULL = 1, 1, 1                           */
+                             code * descale); required (pass 1, 1, 1 explicitly for
+                             unscaled codes).  Must be NULL for GNA_BF16.           */
 } gna_options;
 
 /* ------------------------------------------------------------ layout ---- */
@@ -113,6 +116,14 @@ gna_status gna_tile_shape(const int dims[3], int tile[3]);
 /* Number of elements of one tiled tensor: B*heads*nT*nH*nW*128*head_dim
  * (returns -1 on invalid arguments; tile NULL = default tile). */
 int64_t gna_tiled_elems(int B, int heads, const int dims[3], const int tile[3], int head_dim);
+
+/* Elements of one tensor that gna_permute / gna_permute_v write for these
+ * sizes under the default tile: gna_tiled_elems(B, heads, dims, NULL,
+ * head_dim), the size to allocate for q, k, v_value and out of gna_forward.
+ * Returns 0 on invalid arguments.  GNA page §2.2 (the tokens are permuted
+ * into tile order before attention) and §1.1 (fixed-size tiles: the grid is
+ * padded up to whole tiles). */
+size_t gna_permuted_elems(int B, int heads, const int dims[3], int head_dim);
 
 /* Raster -> tiled (zero padding) and tiled -> raster (padding dropped).
  * src and dst must not overlap.  Any head_dim >= 1 with head_dim * element
@@ -150,21 +161,40 @@ gna_status gna_unpermute_v_tiled(const void* src, void* dst, int B, int heads, c
 /* GNA forward pass (GNA page §1.1 window rule, §2.1 kernel structure).
  *
  * q, k    : tiled [B, heads, tiles, 128, head_dim] (gna_permute)
- * v       : value layout [B, heads, tiles, head_dim, 128] (gna_permute_v)
- *           q, k, v all GNA_BF16 or all GNA_FP8_E4M3
- * out     : tiled [B, heads, tiles, 128, head_dim] bfloat16 (also for fp8
- *           inputs); padding rows are written as zero
+ * v_value : V in the VALUE layout [B, heads, tiles, head_dim, 128]
+ *           (gna_permute_v), NOT the tiled layout of q and k.  The two layouts
+ *           have the same size and cannot be told apart from the pointer: a
+ *           tiled V gives wrong results without any error.  (The value layout
+ *           lets P V read V in the operand order the tensor core streams at
+ *           full rate; see the layout notes above.)
+ *           q, k, v_value all GNA_BF16 (gna_forward_fp8 for GNA_FP8_E4M3)
+ * out     : tiled [B, heads, tiles, 128, head_dim] bfloat16; padding rows are
+ *           written as zero
  * lse     : tiled [B, heads, tiles, 128] float32, natural log; may be NULL
  * dims, window, stride : per dimension (T, H, W); 1 <= stride <= window <= dims
- * head_dim: 32, 64 or 128 (GNA_FP8_E4M3: 128)
- * Uses the default tile, GNA_LEADER_CENTER, scale 1/sqrt(head_dim) and unit
- * fp8 descales.  Asynchronous on `stream`. */
-gna_status gna_forward(const void* q, const void* k, const void* v, void* out, float* lse,
+ * head_dim: 32, 64 or 128
+ * Uses the default tile, GNA_LEADER_CENTER and scale 1/sqrt(head_dim).
+ * dtype must be GNA_BF16: e4m3 codes need their per-tensor descales, so
+ * GNA_FP8_E4M3 returns GNA_ERR_INVALID_ARG here (use gna_forward_fp8).
+ * Asynchronous on `stream`. */
+gna_status gna_forward(const void* q, const void* k, const void* v_value, void* out, float* lse,
                        int B, int heads, const int dims[3], const int window[3], const int stride[3],
                        int head_dim, gna_dtype dtype, void* stream);
 
-/* gna_forward with explicit options (tile, leader rule, scale, fp8 descales). */
-gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out, float* lse,
+/* gna_forward on float8 e4m3 codes (GNA page §1.2 and §2.1: the FP8 mode).
+ * q, k, v_value hold e4m3 codes in the layouts of gna_forward; descale_qkv is
+ * a device pointer to 3 floats, the per-tensor dequantisation scales of q, k
+ * and v (value = code * descale, e.g. amax / 448 of each tensor).  The q and
+ * k scales fold into the softmax scale and the v scale into the epilogue; P
+ * is rounded to e4m3 for P V; out stays bfloat16.  head_dim 128.  NULL
+ * descale_qkv is GNA_ERR_INVALID_ARG. */
+gna_status gna_forward_fp8(const void* q, const void* k, const void* v_value, void* out, float* lse,
+                           int B, int heads, const int dims[3], const int window[3], const int stride[3],
+                           int head_dim, const float* descale_qkv, void* stream);
+
+/* gna_forward with explicit options (tile, leader rule, scale, fp8 descales),
+ * for either dtype; GNA_FP8_E4M3 requires opt->descale. */
+gna_status gna_forward_ex(const void* q, const void* k, const void* v_value, void* out, float* lse,
                           int B, int heads, const int dims[3], const int window[3], const int stride[3],
                           int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
 
@@ -176,13 +206,13 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out
  * are neither read nor written.
  *
  * q, k    : raster [B, T, H, W, heads, head_dim], row stride heads*head_dim
- * v       : value layout [B, heads, tiles, head_dim, 128] (gna_permute_v_tiled
- *           with the same tile)
+ * v_value : value layout [B, heads, tiles, head_dim, 128] (gna_permute_v_tiled
+ *           with the same tile; not raster)
  * out     : raster [B, T, H, W, heads, head_dim] bfloat16
  * lse     : raster [B, T, H, W, heads] float32, natural log; may be NULL
  * Everything else as gna_forward_ex; opt may be NULL.  All pointers 16-byte
  * aligned.  GNA_ERR_INVALID_ARG / GNA_ERR_UNSUPPORTED as gna_forward_ex. */
-gna_status gna_forward_raster(const void* q, const void* k, const void* v, void* out, float* lse,
+gna_status gna_forward_raster(const void* q, const void* k, const void* v_value, void* out, float* lse,
                               int B, int heads, const int dims[3], const int window[3], const int stride[3],
                               int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
 
@@ -276,6 +306,16 @@ gna_status gna_schedule_step(int step, int num_steps, int full_steps, const int 
 gna_status gna_get_status(void* stream);
 
 const char* gna_status_string(gna_status s);
+
+/* TEST ONLY: failure injection for the tests of the bounded waits.  Makes the
+ * TMA producer of every later launch of one kernel skip the K/V load of loop
+ * iteration `kv_index`, so that the consumers' bounded waits run out and the
+ * kernel reports GNA_ERR_TIMEOUT through gna_get_status (after about two
+ * seconds, with that launch's outputs incomplete).  kernel 0 = the forward,
+ * 1 = the dQ backward; kv_index < 0 turns the injection off (the state at
+ * load).  Process-wide; nothing else sets it.  GNA_ERR_INVALID_ARG for an
+ * unknown kernel. */
+gna_status gna_test_skip_kv_load(int kernel, int kv_index);
 
 /* Message of the last error returned on the calling thread ("" if none). */
 const char* gna_last_error(void);

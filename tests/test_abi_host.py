@@ -63,7 +63,7 @@ FAKE = 0x10000   # never dereferenced: every call below fails validation first
     (dict(dims=(0, 16, 16)), G.GNA_ERR_INVALID_ARG),
     (dict(head_dim=96), G.GNA_ERR_UNSUPPORTED),
     (dict(dtype=G.GNA_F32), G.GNA_ERR_INVALID_ARG),
-    (dict(dtype=G.GNA_FP8_E4M3, head_dim=64), G.GNA_ERR_UNSUPPORTED),
+    (dict(dtype=G.GNA_FP8_E4M3, head_dim=128), G.GNA_ERR_INVALID_ARG),   # e4m3 needs descales
     (dict(B=0), G.GNA_ERR_INVALID_ARG),
 ])
 def test_forward_rejects_bad_arguments_on_host(L, kwargs, status):
@@ -86,6 +86,50 @@ def test_forward_ex_rejects_bad_options(L):
         opt.leader_rule = rule
         opt.scale = scale
         assert L.gna_forward_ex(*args, ctypes.byref(opt), None) == G.GNA_ERR_INVALID_ARG
+
+
+def test_survey_boundary_calls_exist_and_validate_on_host(L):
+    """Every call of the planned C ABI is exported under its name and checks its
+    arguments before launching anything."""
+    for name in ("gna_forward", "gna_forward_fp8", "gna_permute", "gna_unpermute", "gna_tile_shape",
+                 "gna_permuted_elems", "gna_get_status", "gna_status_string"):
+        assert hasattr(L, name), name
+    dims = I3(30, 48, 80)
+    assert L.gna_permuted_elems(1, 24, dims, 128) == G.gna_tiled_elems(1, 24, (30, 48, 80), 128)
+    assert L.gna_permuted_elems(2, 3, I3(3, 5, 7), 16) == G.gna_tiled_elems(2, 3, (3, 5, 7), 16)
+    assert G.gna_permuted_elems(1, 2, (1, 16, 16), 32) == 2 * 2 * 128 * 32
+    for bad in ((0, 1, I3(1, 4, 4), 8), (1, 1, I3(0, 4, 4), 8), (1, 1, I3(1, 4, 4), 0)):
+        assert L.gna_permuted_elems(*bad) == 0
+    geom = (1, 2, I3(30, 48, 80), I3(16, 32, 48), I3(1, 1, 1))
+    # e4m3 without descales is refused by every forward entry point
+    assert L.gna_forward_fp8(FAKE, FAKE, FAKE, FAKE, None, *geom, 128, None, None) == G.GNA_ERR_INVALID_ARG
+    assert L.gna_forward(FAKE, FAKE, FAKE, FAKE, None, *geom, 128, G.GNA_FP8_E4M3, None) == G.GNA_ERR_INVALID_ARG
+    assert "gna_forward_fp8" in L.gna_last_error().decode()
+    opt = G.GNAOptions()
+    assert L.gna_forward_ex(FAKE, FAKE, FAKE, FAKE, None, *geom, 128, G.GNA_FP8_E4M3, ctypes.byref(opt),
+                            None) == G.GNA_ERR_INVALID_ARG
+    assert L.gna_forward_raster(FAKE, FAKE, FAKE, FAKE, None, *geom, 128, G.GNA_FP8_E4M3, None,
+                                None) == G.GNA_ERR_INVALID_ARG
+    # gna_forward_fp8 with descales validates the rest like gna_forward
+    assert L.gna_forward_fp8(FAKE, FAKE, FAKE, FAKE, None, 1, 2, I3(30, 48, 80), I3(16, 64, 48), I3(1, 1, 1),
+                             128, FAKE, None) == G.GNA_ERR_INVALID_ARG
+    assert L.gna_forward_fp8(FAKE, FAKE, FAKE, FAKE, None, *geom, 64, FAKE, None) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_forward_fp8(FAKE + 8, FAKE, FAKE, FAKE, None, *geom, 128, FAKE, None) == G.GNA_ERR_INVALID_ARG
+    # descales are refused for bf16
+    opt.descale = FAKE
+    assert L.gna_forward_ex(FAKE, FAKE, FAKE, FAKE, None, *geom, 128, G.GNA_BF16, ctypes.byref(opt),
+                            None) == G.GNA_ERR_INVALID_ARG
+
+
+def test_failure_injection_is_an_explicit_call(L):
+    """The skipped-load hook of the timeout tests is set only through its entry
+    point, never from the environment."""
+    assert L.gna_test_skip_kv_load(2, 1) == G.GNA_ERR_INVALID_ARG
+    for kernel in (0, 1):
+        assert L.gna_test_skip_kv_load(kernel, 3) == G.GNA_OK
+        assert L.gna_test_skip_kv_load(kernel, -1) == G.GNA_OK
+    src = open(os.path.join(ROOT, "dimensional_sparse_attention_gna_b300", "csrc", "gna_api.cu")).read()
+    assert "getenv" not in src
 
 
 def test_forward_raster_rejects_bad_arguments_on_host(L):
@@ -245,7 +289,7 @@ def test_binding_checks_tensor_sizes_before_any_call():
     with pytest.raises(ValueError, match="q holds"):
         G.gna_forward_raster(small_raster, ok_raster, ok_tiled, ok_raster, None, B, heads, dims, (1, 5, 5),
                              (1, 1, 1), d)
-    with pytest.raises(ValueError, match="v holds"):
+    with pytest.raises(ValueError, match="v_value holds"):
         G.gna_forward_raster(ok_raster, ok_raster, small_tiled, ok_raster, None, B, heads, dims, (1, 5, 5),
                              (1, 1, 1), d)
     # sizes right: the next refusal is the device check (CPU tensors)

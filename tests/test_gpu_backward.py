@@ -104,16 +104,15 @@ def test_backward_abandoned_wait_reports_timeout_and_context_survives():
     """The dQ producer skips one KV load (test hook): the MMA warp's bounded wait
     gives up, the kernel exits, and the host reads GNA_ERR_TIMEOUT.  The next
     backward on the same context is correct again."""
-    import os
     dims, window, stride, d = (1, 16, 16), (1, 5, 5), (1, 1, 1), 128
     q, k, v, dout = (to_bf16(normal_raster(8300 + i, 1, dims, 1, d)) for i in range(4))
-    os.environ["GNA_TEST_SKIP_BWD_LOAD"] = "1"
+    G.gna_test_skip_kv_load(1, 1)
     try:
         with pytest.raises(G.GNAError) as ei:
             gpu_backward(q, k, v, dout, dims, window, stride)
         assert ei.value.status == G.GNA_ERR_TIMEOUT
     finally:
-        del os.environ["GNA_TEST_SKIP_BWD_LOAD"]
+        G.gna_test_skip_kv_load(1, -1)
     G.gna_get_status()   # cleared
     _check_grads(8300, 1, 1, dims, window, stride)
 

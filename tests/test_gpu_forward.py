@@ -169,13 +169,13 @@ def test_abandoned_wait_reports_timeout_and_context_survives():
     call on the same context works."""
     dims, window, stride = (1, 16, 16), (1, 5, 5), (1, 1, 1)
     q, k, v = bf16_inputs(4000, 1, dims, 1, 32)
-    os.environ["GNA_TEST_SKIP_KV_LOAD"] = "1"
+    G.gna_test_skip_kv_load(0, 1)
     try:
         with pytest.raises(G.GNAError) as ei:
             gpu_gna(q, k, v, dims, window, stride)
         assert ei.value.status == G.GNA_ERR_TIMEOUT
     finally:
-        del os.environ["GNA_TEST_SKIP_KV_LOAD"]
+        G.gna_test_skip_kv_load(0, -1)
     G.gna_get_status()   # cleared
     out, lse = gpu_gna(q, k, v, dims, window, stride)
     o_ref, l_ref = oracle.forward_c(exact_f32(q), exact_f32(k), exact_f32(v), dims, window, stride)
