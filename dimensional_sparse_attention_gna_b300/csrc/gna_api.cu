@@ -267,6 +267,21 @@ gna_status permute_common(const void* src, void* dst, int B, int heads, const in
 
 }  // namespace
 
+namespace gna {
+
+gna_status api_fail(gna_status s, const char* fmt, ...)
+{
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+}  // namespace gna
+
 extern "C" {
 
 int gna_version(void) { return GNA_VERSION; }

@@ -5,7 +5,13 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "../../include/gna.h"
+
 namespace gna {
+
+// Records a printf-style message as the calling thread's gna_last_error() and
+// returns `s` (defined with the C ABI in gna_api.cu).
+gna_status api_fail(gna_status s, const char* fmt, ...);
 
 // Geometry of one permute / unpermute launch.
 struct PermuteGeom {

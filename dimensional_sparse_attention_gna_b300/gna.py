@@ -107,6 +107,9 @@ def lib() -> ctypes.CDLL:
         L.gna_backward_dkdv.restype = st
         L.gna_backward_dkdv.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _INT,
                                         ctypes.POINTER(GNAOptions), _P]
+        L.gna_backward_noalloc.restype = st
+        L.gna_backward_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT,
+                                           _INT, ctypes.POINTER(GNAOptions), _P]
         L.gna_tile_stats.restype = st
         L.gna_tile_stats.argtypes = [_I3, _I3, _I3, _P, _INT, ctypes.POINTER(i64), ctypes.POINTER(i64),
                                      ctypes.POINTER(i64)]
@@ -433,6 +436,32 @@ def gna_backward_dkdv(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dout: t
     _check(lib().gna_backward_dkdv(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(lse), _ptr(delta), _ptr(dk),
                                    _ptr(dv), B, heads, _I3(*dims), _I3(*window), _I3(*stride), head_dim, GNA_BF16,
                                    ctypes.byref(opt), _stream_ptr(stream, dev)))
+
+
+def gna_backward_noalloc(q: torch.Tensor, k: torch.Tensor, k_value: torch.Tensor, v: torch.Tensor,
+                         out: torch.Tensor, dout: torch.Tensor, lse: torch.Tensor, dq: torch.Tensor, dk: torch.Tensor,
+                         dv: torch.Tensor, B: int, heads: int, dims, window, stride, head_dim: int, *, tile=None,
+                         leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, stream=None):
+    """dq, dk and dv in one call that allocates nothing (see ``include/gna.h``):
+    for callers that cannot allocate the delta workspace themselves.  The
+    library keeps delta in a fixed device array (at most 2^22 tiled rows) that
+    all calls share: calls must not overlap on the GPU."""
+    for name, t in (("q", q), ("k", k), ("k_value", k_value), ("v", v), ("out", out), ("dout", dout), ("dq", dq),
+                    ("dk", dk), ("dv", dv)):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bfloat16")
+    if lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
+    dev = _need(q=(q, nt), k=(k, nt), k_value=(k_value, nt), v=(v, nt), out=(out, nt), dout=(dout, nt),
+                lse=(lse, nt // head_dim), dq=(dq, nt), dk=(dk, nt), dv=(dv, nt))
+    opt = GNAOptions()
+    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+    opt.leader_rule = leader_rule
+    opt.scale = scale
+    _check(lib().gna_backward_noalloc(_ptr(q), _ptr(k), _ptr(k_value), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), B, heads, _I3(*dims), _I3(*window),
+                                      _I3(*stride), head_dim, GNA_BF16, ctypes.byref(opt), _stream_ptr(stream, dev)))
 
 
 def gna_schedule_step(step: int, num_steps: int, full_steps: int, dims, window, stride):

@@ -259,6 +259,43 @@ gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, co
                            int heads, const int dims[3], const int window[3], const int stride[3],
                            int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
 
+/* gna_backward_noalloc: the three backward calls above in one, for callers
+ * that cannot allocate device memory.  The pages have no counterpart of this
+ * call; it exists for a need of the callers, not of the method.
+ *
+ * gna_backward_dq and gna_backward_dkdv read a caller-owned float workspace
+ * (delta, one value per tiled row).  Callers that cannot provide it are, for
+ * example, code that runs inside a framework's memory pool or arena that owns
+ * every device allocation, a process held to a fixed allocation budget, and
+ * host code that must not call cudaMalloc (which can synchronise the device
+ * and fail at any moment).  This call keeps delta in a fixed array of the
+ * library's own device memory instead.  It allocates nothing and calls no
+ * allocating routine; the caller still passes every input and output.
+ *
+ *   q, k, v, dout : tiled bfloat16 (as gna_backward_dq); k_value: k in the
+ *                   value layout; out, lse: the forward's tiled out and lse
+ *   dq, dk, dv    : tiled bfloat16, written
+ *   other arguments as gna_backward_dq; bf16 with head_dim 128 only
+ *
+ * Limit: B * heads * tiles * 128 (the tiled rows) must not exceed 2^22 =
+ * 4,194,304; larger problems return GNA_ERR_INVALID_ARG before anything is
+ * launched (use the three calls above with your own delta).  The array, 16
+ * MiB, occupies global memory on every GPU that loads the library until the
+ * process exits.
+ *
+ * The first call on a device looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array and leaves its delta
+ * values there; each call writes all the entries it reads before reading
+ * them, so nothing needs clearing between calls.  Calls whose kernels overlap
+ * on the GPU (on different streams, or from different threads) race on the
+ * array and give wrong gradients: serialise them.  Asynchronous on `stream`;
+ * errors as gna_backward_dq. */
+gna_status gna_backward_noalloc(const void* q, const void* k, const void* k_value, const void* v,
+                                const void* out, const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                int B, int heads, const int dims[3], const int window[3], const int stride[3],
+                                int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
+
 /* ------------------------------------------------------------ planning ---- */
 
 /* Tile statistics of one (b, head) plane under the given tile (NULL =
