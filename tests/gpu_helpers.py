@@ -18,6 +18,17 @@ TOL_BF16_OUT = 2e-2
 TOL_BF16_LSE = 1e-2
 TOL_FP8 = 6e-2
 
+# Regression gates on the relative RMS error of out, far tighter than the max-abs
+# bars above (which a shifted window could pass at large window volumes): about
+# twice the largest value measured on a B300 over every parity test (bf16
+# 2.35e-3, set by the bf16 rounding of out and P; e4m3 2.62e-2, set by the e4m3
+# rounding of P).  Gradients: relative RMS measured <= 2.49e-3, largest error
+# 0.53 % of the largest gradient.
+REL_RMS_BF16 = 5e-3
+REL_RMS_FP8 = 5e-2
+REL_RMS_GRAD = 5e-3
+MAX_ERR_GRAD = 1e-2          # of max |gradient|
+
 
 def oracle_threads() -> int:
     return max(1, (os.cpu_count() or 1))
@@ -57,11 +68,28 @@ def bf16_inputs(seed: int, B, dims, heads, d):
     return q, k, v
 
 
-def compare(out, lse, o_ref, l_ref, tol_out, tol_lse):
+def record_parity(**fields):
+    """Append one JSON line of measured parity figures (with the running test's
+    id) to the file named by GNA_PARITY_RECORD, when that variable is set: the
+    source of the committed per-configuration parity summary."""
+    path = os.environ.get("GNA_PARITY_RECORD")
+    if not path:
+        return
+    import json
+    rec = {"test": os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]}
+    rec.update({k: (float(v) if isinstance(v, (np.floating, float)) else v) for k, v in fields.items()})
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")
+
+
+def compare(out, lse, o_ref, l_ref, tol_out, tol_lse, **record):
     d_out = np.abs(out.astype(np.float64) - o_ref)
     d_lse = np.abs(lse.astype(np.float64) - l_ref)
     rel = math.sqrt(float((d_out ** 2).mean()) / max(float((o_ref ** 2).mean()), 1e-30))
     info = f"max|dout|={d_out.max():.3e} max|dlse|={d_lse.max():.3e} relRMS={rel:.3e}"
+    record.setdefault("dtype", "fp8" if tol_out >= TOL_FP8 else "bf16")
+    record_parity(kind="forward", max_abs_out=float(d_out.max()), max_abs_lse=float(d_lse.max()), rel_rms_out=rel,
+                  n_queries=int(np.prod(lse.shape)), **record)
     assert np.isfinite(out).all() and np.isfinite(lse).all(), info
     assert d_out.max() <= tol_out, info
     assert d_lse.max() <= tol_lse, info

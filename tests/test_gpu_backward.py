@@ -5,8 +5,9 @@ dk and dv compared.
 The GPU path reads the bf16 out and lse of its own forward; the oracle
 recomputes everything in float64 from the same bf16 inputs.  The differences
 come from bf16 dS, bf16 out in delta and the bf16 result, so the bar is a
-relative one: relative RMS < 1e-2 and max |error| <= 2 % of max |gradient|
-(measured: relative RMS ~2.4e-3, max |error| ~0.5 %, the size of bf16 rounding).
+relative one: relative RMS < 5e-3 and max |error| <= 1 % of max |gradient|
+(measured: relative RMS <= 2.5e-3, max |error| <= 0.53 %, the size of bf16
+rounding).
 """
 import numpy as np
 import pytest
@@ -15,7 +16,7 @@ import torch
 import oracle
 from dimensional_sparse_attention_gna_b300 import gna as G
 from synthetic_inputs import exact_f32, normal_raster, to_bf16
-from tests.gpu_helpers import sample_queries
+from tests.gpu_helpers import MAX_ERR_GRAD, REL_RMS_GRAD, record_parity, sample_queries
 
 pytestmark = pytest.mark.gpu
 
@@ -68,9 +69,12 @@ def _check_grads(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEA
         rel = float(np.sqrt((err ** 2).mean() / (r ** 2).mean()))
         info = f"{name}: max|err|={err.max():.3e} max|ref|={np.abs(r).max():.3e} relRMS={rel:.3e}"
         print(info)
+        record_parity(kind="backward", grad=name, seed=seed, dims=list(dims), window=list(window),
+                      stride=list(stride), heads=heads, B=B, max_abs_err=float(err.max()),
+                      max_abs_ref=float(np.abs(r).max()), rel_rms=rel)
         assert np.isfinite(g).all(), info
-        assert rel < 1e-2, info
-        assert err.max() <= 0.02 * np.abs(r).max(), info
+        assert rel < REL_RMS_GRAD, info
+        assert err.max() <= MAX_ERR_GRAD * np.abs(r).max(), info
 
 
 @pytest.mark.parametrize("B,heads,dims,window,stride,tile,rule", [
@@ -117,26 +121,48 @@ def test_backward_abandoned_wait_reports_timeout_and_context_survives():
     _check_grads(8300, 1, 1, dims, window, stride)
 
 
+def _compare_sampled(name, got, ref, **rec):
+    err = np.abs(got.astype(np.float64) - ref)
+    rel = float(np.sqrt((err ** 2).mean() / (ref ** 2).mean()))
+    info = f"{name}: max|err|={err.max():.3e} max|ref|={np.abs(ref).max():.3e} relRMS={rel:.3e}"
+    print(info)
+    record_parity(kind="backward", grad=name, max_abs_err=float(err.max()), max_abs_ref=float(np.abs(ref).max()),
+                  rel_rms=rel, sampled=True, **rec)
+    assert np.isfinite(got).all(), info
+    assert rel < REL_RMS_GRAD and err.max() <= MAX_ERR_GRAD * np.abs(ref).max(), info
+
+
 def test_gradients_video_720p_sampled_and_identities():
     """Full-size 3-D video workload (30x48x80 tokens, 24 heads, d=128, window
-    16x32x48, stride 1): dq at sampled queries against the oracle, and dv through
-    an identity of the derivative that holds at any size: sum_j dv_j =
-    sum_i dout_i per head and feature (each query's probabilities sum to 1).
-    Measured: the identity holds to ~1e-4 of the sums.  dk is compared element by
-    element on the mid-size grid above."""
+    16x32x48, stride 1), every gradient compared with the oracle at samples:
+    dq at sampled queries (corner Q tiles of the first and last head plus
+    random queries of any head), dk and dv at sampled keys (every key of the
+    corner KV tiles of the first and last head plus random keys of those two
+    heads: the key-side oracle recomputes lse and delta for every query of each
+    plane it touches, so the keys stay in two planes).  dv also meets an
+    identity of the derivative that holds at any size: sum_j dv_j = sum_i
+    dout_i per head and feature (each query's probabilities sum to 1)."""
     B, heads, dims, window, stride, d = 1, 24, (30, 48, 80), (16, 32, 48), (1, 1, 1), 128
     q, k, v, dout = (to_bf16(normal_raster(8400 + i, B, dims, heads, d)) for i in range(4))
     (dq, dk, dv), _ = gpu_backward(q, k, v, dout, dims, window, stride)
+    qf, kf, vf, gf = (exact_f32(x) for x in (q, k, v, dout))
+    geo = dict(seed=8400, dims=list(dims), window=list(window), stride=list(stride), heads=heads, B=B)
+    tile = G.gna_tile_shape(dims)
     rng = np.random.default_rng(8400)
-    sel = sample_queries(rng, B, heads, dims, G.gna_tile_shape(dims), 128)
+    sel = sample_queries(rng, B, heads, dims, tile, 128)
     ids = oracle.query_ids(sel[:, 0], sel[:, 1], sel[:, 2], sel[:, 3], sel[:, 4], heads, dims)
-    ref = oracle.backward_dq_c(exact_f32(q), exact_f32(k), exact_f32(v), exact_f32(dout), dims, window, stride, ids)
-    got = dq[sel[:, 0], sel[:, 2], sel[:, 3], sel[:, 4], sel[:, 1]].astype(np.float64)
-    err = np.abs(got - ref)
-    rel = float(np.sqrt((err ** 2).mean() / (ref ** 2).mean()))
-    assert rel < 1e-2 and err.max() <= 0.02 * np.abs(ref).max(), (rel, err.max())
+    ref = oracle.backward_dq_c(qf, kf, vf, gf, dims, window, stride, ids)
+    _compare_sampled("dq", dq[sel[:, 0], sel[:, 2], sel[:, 3], sel[:, 4], sel[:, 1]], ref, **geo)
+
+    ksel = sample_queries(rng, B, heads, dims, tile, 256)
+    ksel[len(ksel) - 256:, 1] = rng.choice([0, heads - 1], 256)       # random keys in the corner heads' planes
+    kids = oracle.query_ids(ksel[:, 0], ksel[:, 1], ksel[:, 2], ksel[:, 3], ksel[:, 4], heads, dims)
+    dk_ref, dv_ref = oracle.backward_kv_c(qf, kf, vf, gf, dims, window, stride, kids)
+    at = (ksel[:, 0], ksel[:, 2], ksel[:, 3], ksel[:, 4], ksel[:, 1])
+    _compare_sampled("dk", dk[at], dk_ref, **geo)
+    _compare_sampled("dv", dv[at], dv_ref, **geo)
+
     axes = (0, 1, 2, 3)
-    dsum = exact_f32(dout).astype(np.float64).sum(axis=axes)          # [heads, d]
+    dsum = gf.astype(np.float64).sum(axis=axes)          # [heads, d]
     gap = np.abs(dv.astype(np.float64).sum(axis=axes) - dsum)
     assert gap.max() <= 1e-3 * np.abs(dsum).max(), (gap.max(), np.abs(dsum).max())
-    assert np.isfinite(dk).all()

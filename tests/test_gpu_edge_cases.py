@@ -13,7 +13,8 @@ import torch
 
 import oracle
 from synthetic_inputs import exact_f32, normal_raster, quantize_e4m3, to_bf16
-from tests.gpu_helpers import TOL_BF16_LSE, TOL_BF16_OUT, TOL_FP8, bf16_inputs, compare, gpu_gna, oracle_threads
+from tests.gpu_helpers import (REL_RMS_BF16, REL_RMS_FP8, TOL_BF16_LSE, TOL_BF16_OUT, TOL_FP8, bf16_inputs, compare,
+                               gpu_gna, oracle_threads)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,21 +57,21 @@ def test_single_token_grid():
 def test_degenerate_geometries(dims, window, stride):
     q, k, v = bf16_inputs(5100 + sum(dims), 1, dims, 2, 64)
     _, _, rel, info = _parity(q, k, v, dims, window, stride)
-    assert rel < 1.5e-2, info
+    assert rel < REL_RMS_BF16, info
 
 
 def test_every_tile_padded_many_batches():
     dims = (3, 5, 7)                               # default tile pads every dimension
     q, k, v = bf16_inputs(5200, 3, dims, 1, 128)
     _, _, rel, info = _parity(q, k, v, dims, (3, 3, 5), (1, 2, 2))
-    assert rel < 1.5e-2, info
+    assert rel < REL_RMS_BF16, info
 
 
 def test_many_heads():
     dims = (1, 8, 24)
     q, k, v = bf16_inputs(5300, 1, dims, 64, 64)
     _, _, rel, info = _parity(q, k, v, dims, (1, 5, 9), (1, 1, 3))
-    assert rel < 1.5e-2, info
+    assert rel < REL_RMS_BF16, info
 
 
 def test_e4m3_ragged_grid_all_queries():
@@ -79,7 +80,7 @@ def test_e4m3_ragged_grid_all_queries():
     (q, sq), (k, sk), (v, sv) = qs
     _, _, rel, info = _parity(q, k, v, dims, (4, 9, 8), (2, 3, 8), scales=(sq, sk, sv), tol_out=TOL_FP8,
                               tol_lse=TOL_FP8, descale=(sq, sk, sv))
-    assert rel < 0.1, info
+    assert rel < REL_RMS_FP8, info
 
 
 @pytest.mark.parametrize("amp", [6.0, 24.0])
@@ -93,7 +94,7 @@ def test_large_scores_lazy_rescale(amp):
     k = to_bf16(normal_raster(5501, 1, dims, 2, d))
     v = to_bf16(normal_raster(5502, 1, dims, 2, d))
     out, lse, rel, info = _parity(q, k, v, dims, (3, 9, 17), (1, 1, 1), tol_lse=1e-2 * amp)
-    assert rel < 1.5e-2, info
+    assert rel < REL_RMS_BF16, info
 
 
 def test_without_lse_and_on_a_side_stream():

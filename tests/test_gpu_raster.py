@@ -14,7 +14,7 @@ import torch
 import oracle
 from dimensional_sparse_attention_gna_b300 import gna as G
 from synthetic_inputs import exact_f32, normal_raster, quantize_e4m3
-from tests.gpu_helpers import (TOL_BF16_LSE, TOL_BF16_OUT, TOL_FP8, bf16_inputs, compare, gpu_gna, oracle_threads,
+from tests.gpu_helpers import (REL_RMS_BF16, REL_RMS_FP8, TOL_BF16_LSE, TOL_BF16_OUT, TOL_FP8, bf16_inputs, compare, gpu_gna, oracle_threads,
                                sample_queries)
 
 pytestmark = pytest.mark.gpu
@@ -61,7 +61,7 @@ def test_raster_small_grids_all_queries(d, dims, window, stride, tile):
     o_ref, l_ref = oracle.forward_c(exact_f32(q), exact_f32(k), exact_f32(v), dims, window, stride,
                                     threads=oracle_threads())
     rel, info = compare(out, lse, o_ref, l_ref, TOL_BF16_OUT, TOL_BF16_LSE)
-    assert rel < 1.5e-2, info
+    assert rel < REL_RMS_BF16, info
     out_t, lse_t = gpu_gna(q, k, v, dims, window, stride, tile=tile)
     np.testing.assert_array_equal(out, out_t)
     np.testing.assert_array_equal(lse, lse_t)
@@ -83,7 +83,7 @@ def test_raster_e4m3_ragged():
     o_ref, l_ref = oracle.forward_c(exact_f32(q), exact_f32(k), exact_f32(v), dims, (4, 9, 8), (2, 3, 8),
                                     tensor_scales=(sq, sk, sv), threads=oracle_threads())
     rel, info = compare(out, lse, o_ref, l_ref, TOL_FP8, TOL_FP8)
-    assert rel < 0.1, info
+    assert rel < REL_RMS_FP8, info
 
 
 @pytest.mark.parametrize("stride", [(1, 1, 1), (16, 8, 8)])
@@ -103,4 +103,4 @@ def test_raster_video_720p_latent_sampled(stride):
     o_gpu = out[sel[:, 0], sel[:, 2], sel[:, 3], sel[:, 4], sel[:, 1]]
     l_gpu = lse[sel[:, 0], sel[:, 2], sel[:, 3], sel[:, 4], sel[:, 1]]
     rel, info = compare(o_gpu, l_gpu, o_ref, l_ref, TOL_BF16_OUT, TOL_BF16_LSE)
-    assert rel < 1.5e-2, info
+    assert rel < REL_RMS_BF16, info
