@@ -37,7 +37,7 @@
 
 namespace gna {
 
-__device__ int g_bwd_status = 0;
+__device__ int g_bwd_status = 0;     // GNA_ERR_TIMEOUT once any CTA gave up a wait (every wait also stops then)
 
 namespace {
 
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             const int s = j % kBStages;
             const int64_t tile = kv_tile_base + (kc[0] * p.nt[1] + kc[1]) * p.nt[2] + kc[2];
             if (j >= kBStages &&
-                !__all_sync(0xffffffffu, mbar_wait(bar(bars.empty[s]), ((j / kBStages) & 1) ^ 1, &abort_flag))) {
+                !__all_sync(0xffffffffu, mbar_wait(bar(bars.empty[s]), ((j / kBStages) & 1) ^ 1, &abort_flag, &g_bwd_status))) {
                 early = true;
                 break;
             }
@@ -211,10 +211,10 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         const uint32_t tDQ = tmem + kColDQ, tS = tmem + kColS, tDP = tmem + kColDP;
         const uint32_t tQ = tmem + kColQ, tDO = tmem + kColDO;
         const uint64_t d0 = make_smem_desc(s_base, 16, 8 * 128, kSwizzle128B);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.qdo_full), 0, &abort_flag));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.qdo_full), 0, &abort_flag, &g_bwd_status));
         for (int j = 0; ok && j < n_kv; ++j) {
             const int s = j % kBStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (j / kBStages) & 1, &abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (j / kBStages) & 1, &abort_flag, &g_bwd_status))) {
                 ok = false;
                 break;
             }
@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
                 mma_commit(bar(bars.sdp_full));
             }
             __syncwarp();
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.ds_full), j & 1, &abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.ds_full), j & 1, &abort_flag, &g_bwd_status))) {
                 ok = false;
                 break;
             }
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         bool ok = true;
         int kc[3] = {box.k0[0], box.k0[1], box.k0[2]};
         for (int j = 0; j < n_kv && ok; ++j, bwd_odometer(kc, box)) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.sdp_full), j & 1, &abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.sdp_full), j & 1, &abort_flag, &g_bwd_status));
             if (!ok) {
                 bwd_raise(&abort_flag);
                 break;
@@ -368,7 +368,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
 
         // ------------------------------------------------------------ epilogue
         if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.dq_final), 0, &abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.dq_final), 0, &abort_flag, &g_bwd_status));
             if (!ok) bwd_raise(&abort_flag);
         }
         if (ok) {
@@ -526,7 +526,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             const int s = i % kBStages;
             const int64_t qtile = plane_base + (qc[0] * p.nt[1] + qc[1]) * p.nt[2] + qc[2];
             if (i >= kBStages &&
-                !__all_sync(0xffffffffu, mbar_wait(bar(bars.empty[s]), ((i / kBStages) & 1) ^ 1, &abort_flag))) {
+                !__all_sync(0xffffffffu, mbar_wait(bar(bars.empty[s]), ((i / kBStages) & 1) ^ 1, &abort_flag, &g_bwd_status))) {
                 early = true;
                 break;
             }
@@ -558,10 +558,10 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         const uint32_t tDV = tmem + kColDV, tDK = tmem + kColDK, tST = tmem + kColST, tDPT = tmem + kColDPT;
         const uint64_t dKj = make_smem_desc(sK, 16, 8 * 128, kSwizzle128B);
         const uint64_t dVj = make_smem_desc(sV, 16, 8 * 128, kSwizzle128B);
-        bool ok = n_q == 0 || __all_sync(0xffffffffu, mbar_wait(bar(bars.kv_full), 0, &abort_flag));
+        bool ok = n_q == 0 || __all_sync(0xffffffffu, mbar_wait(bar(bars.kv_full), 0, &abort_flag, &g_bwd_status));
         for (int i = 0; ok && i < n_q; ++i) {
             const int s = i % kBStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag, &g_bwd_status))) {
                 ok = false;
                 break;
             }
@@ -581,7 +581,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
                 mma_commit(bar(bars.sdp_full));
             }
             __syncwarp();
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.p_full), i & 1, &abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.p_full), i & 1, &abort_flag, &g_bwd_status))) {
                 ok = false;
                 break;
             }
@@ -645,8 +645,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         int qc[3] = {qbox.k0[0], qbox.k0[1], qbox.k0[2]};
         for (int i = 0; i < n_q && ok; ++i, bwd_odometer(qc, qbox)) {
             const int s = i % kBStages;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag)) &&
-                 __all_sync(0xffffffffu, mbar_wait(bar(bars.sdp_full), i & 1, &abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag, &g_bwd_status)) &&
+                 __all_sync(0xffffffffu, mbar_wait(bar(bars.sdp_full), i & 1, &abort_flag, &g_bwd_status));
             if (!ok) {
                 bwd_raise(&abort_flag);
                 break;
@@ -717,7 +717,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
 
         // ------------------------------------------------------------ epilogue
         if (ok && n_q > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.final_), 0, &abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.final_), 0, &abort_flag, &g_bwd_status));
             if (!ok) bwd_raise(&abort_flag);
         }
         if (ok) {

@@ -42,7 +42,9 @@
 // Every mbarrier wait is bounded (see ptx.cuh); a role that gives up raises
 // the CTA abort flag and the device status word, the other roles drop out of
 // their loops, in-flight TMA loads and MMAs are drained (again bounded), TMEM
-// is freed and the CTA exits.
+// is freed and the CTA exits.  The waits of every other CTA of the launch also
+// give up as soon as they see the status word set, so a stuck launch ends after
+// one wait bound instead of one bound per wave of CTAs.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -54,7 +56,7 @@
 
 namespace gna {
 
-__device__ int g_device_status = 0;
+__device__ int g_device_status = 0;     // GNA_ERR_TIMEOUT once any CTA gave up a wait
 
 namespace {
 
@@ -405,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             const uint32_t ph = ((j / NS) & 1) ^ 1;
             const int tile_id = (kc[0] * p.nt[1] + kc[1]) * p.nt[2] + kc[2];
             const int32_t row = static_cast<int32_t>(kv_row_base + static_cast<int64_t>(tile_id) * kTileElems);
-            if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(bar(bars.k_empty[s]), ph, &abort_flag))) {
+            if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(bar(bars.k_empty[s]), ph, &abort_flag, &g_device_status))) {
                 early = true;
                 break;
             }
@@ -428,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             }
             __syncwarp();
             ++k_issued;
-            if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(bar(bars.v_empty[s]), ph, &abort_flag))) {
+            if (j >= NS && !__all_sync(0xffffffffu, mbar_wait(bar(bars.v_empty[s]), ph, &abort_flag, &g_device_status))) {
                 early = true;
                 break;
             }
@@ -463,8 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         const uint64_t dV0 = make_smem_desc(sV, 16, 1024, kSwizzle128B);
         auto issue_pv = [&](int i) -> bool {
             const int s = i % NS;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.v_full[s]), (i / NS) & 1, &abort_flag))) return false;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.p_full[i & 1]), (i >> 1) & 1, &abort_flag))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.v_full[s]), (i / NS) & 1, &abort_flag, &g_device_status))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.p_full[i & 1]), (i >> 1) & 1, &abort_flag, &g_device_status))) return false;
             tc_fence_after();
             if (elect_one_sync()) {
                 const uint64_t dv = dV0 + static_cast<uint64_t>((s * C::kTileBytes) >> 4);
@@ -484,10 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             __syncwarp();
             return true;
         };
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.q_full), 0, &abort_flag));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.q_full), 0, &abort_flag, &g_device_status));
         for (int j = 0; ok && j < n_kv; ++j) {
             const int s = j % NS;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.k_full[s]), (j / NS) & 1, &abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.k_full[s]), (j / NS) & 1, &abort_flag, &g_device_status))) {
                 ok = false;
                 break;
             }
@@ -594,7 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         for (int j = 0; j < n_kv; ++j, advance_odometer(kc, box)) {
             const int sb = j & 1;
             if (ok) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full[sb]), (j >> 1) & 1, &abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full[sb]), (j >> 1) & 1, &abort_flag, &g_device_status));
                 if (!ok) raise_status(&abort_flag);
             }
             const uint32_t t_s = tmem + kColS0 + sb * 128 + lane_addr;
@@ -699,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                     // columns.  S(j) has arrived, so every MMA issued before QK(j),
                     // PV(j-2) included, is complete: o_done is at most one phase
                     // behind and the parity wait is exact.
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_done), (j - 1) & 1, &abort_flag));
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_done), (j - 1) & 1, &abort_flag, &g_device_status));
                     if (!ok) {
                         raise_status(&abort_flag);
                         continue;
@@ -747,7 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             // A parity wait on o_done could pass here while the barrier is
             // still two phases behind (P V of the second-to-last tile not yet
             // done): the last product has a barrier of its own.
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_final), 0, &abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.o_final), 0, &abort_flag, &g_device_status));
             if (!ok) raise_status(&abort_flag);
         }
         // every thread of the pair reaches this exchange (even on failure)

@@ -75,14 +75,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait until the phase with the given parity has completed.  Returns false on
-// timeout or when *abort becomes non-zero (another role of the CTA gave up).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort)
+// timeout, when *abort becomes non-zero (another role of the CTA gave up) or,
+// if given, when *grid_abort becomes non-zero (a CTA of the launch gave up:
+// without it every CTA of a stuck launch would wait out its own bound in turn).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
+                                          const volatile int* grid_abort = nullptr)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (;;) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
+        if (grid_abort != nullptr && *grid_abort) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
