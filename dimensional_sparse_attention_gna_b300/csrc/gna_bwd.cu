@@ -21,9 +21,12 @@
 // TMEM (512 columns): dQ [0, 128), S [128, 256), dP [256, 384), Q [384, 448),
 // dO [448, 512).  Per KV tile: S = Q K^T and dP = dO V^T (A from TMEM), then
 // dQ += dS K with dS (bf16) in TMEM as the A operand: each half writes its 32
-// columns of dS over the front of its own 64 S columns, so the halves never
-// touch each other's scores.  K in the value layout is the K-major B operand
-// of dS K, as V is for P V in the forward.
+// columns of dS over the front of its own 64 dP columns, so the halves never
+// touch each other's values, and the S columns are free as soon as the dS
+// warps hold S in registers: S of the next KV tile is computed while they
+// work.  The element mask of a partial tile is one 32-bit word per 32 key
+// columns (box_mask_word).  K in the value layout is the K-major B operand of
+// dS K, as V is for P V in the forward.
 //
 // Every mbarrier wait is bounded; a role that gives up raises the abort flag
 // and the device status word, and the CTA drains and exits.
@@ -66,8 +69,10 @@ struct BwdBars {
     uint64_t qdo_full;            // Q and dO rows stored in TMEM (8 warps)
     uint64_t full[kBStages];      // K, V, K (value layout) of a KV tile landed
     uint64_t empty[kBStages];     // the KV tile's three MMAs are done
-    uint64_t sdp_full;            // S and dP of the current KV tile are in TMEM
-    uint64_t ds_full;             // dS of the current KV tile is in TMEM (8 warps)
+    uint64_t s_full;              // S of KV tile j is in TMEM (one phase per tile)
+    uint64_t s_free;              // the dS warps hold S(j) in registers: S may take S(j + 1) (8 warps)
+    uint64_t dp_full;             // dP of KV tile j is in TMEM
+    uint64_t ds_full;             // dS of KV tile j is in TMEM, over the front of dP (8 warps)
     uint64_t dq_final;            // the last dQ product is done
     uint64_t drain;
 };
@@ -97,6 +102,42 @@ __device__ __forceinline__ float bwd_exp2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Packed fp32 pairs: (a.x * b.x + c.x, a.y * b.y + c.y), a + b and a * b in one
+// instruction each.
+__device__ __forceinline__ float2 bwd_ffma2(float2 a, float2 b, float2 c)
+{
+    uint64_t ra, rb, rc, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rc) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.ftz.f32x2 %0, %1, %2, %3;" : "=l"(rd) : "l"(ra), "l"(rb), "l"(rc));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
+__device__ __forceinline__ float2 bwd_fadd2(float2 a, float2 b)
+{
+    uint64_t ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("add.rn.ftz.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
+}
+
+__device__ __forceinline__ float2 bwd_fmul2(float2 a, float2 b)
+{
+    uint64_t ra, rb, rd;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ra) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(rb) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.ftz.f32x2 %0, %1, %2;" : "=l"(rd) : "l"(ra), "l"(rb));
+    float2 d;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(d.x), "=f"(d.y) : "l"(rd));
+    return d;
 }
 
 template <int N>
@@ -148,7 +189,9 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             mbar_init(bar(bars.full[s]), 1);
             mbar_init(bar(bars.empty[s]), 1);
         }
-        mbar_init(bar(bars.sdp_full), 1);
+        mbar_init(bar(bars.s_full), 1);
+        mbar_init(bar(bars.s_free), kBSoftmaxWarps);
+        mbar_init(bar(bars.dp_full), 1);
         mbar_init(bar(bars.ds_full), kBSoftmaxWarps);
         mbar_init(bar(bars.dq_final), 1);
         mbar_init(bar(bars.drain), 1);
@@ -211,39 +254,70 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         const uint32_t tDQ = tmem + kColDQ, tS = tmem + kColS, tDP = tmem + kColDP;
         const uint32_t tQ = tmem + kColQ, tDO = tmem + kColDO;
         const uint64_t d0 = make_smem_desc(s_base, 16, 8 * 128, kSwizzle128B);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.qdo_full), 0, &abort_flag, &g_bwd_status));
-        for (int j = 0; ok && j < n_kv; ++j) {
+        // S(j) = Q K(j)^T and dP(j) = dO V(j)^T, from TMEM A operands
+        auto issue_s = [&](int j) -> bool {
             const int s = j % kBStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (j / kBStages) & 1, &abort_flag, &g_bwd_status))) {
-                ok = false;
-                break;
-            }
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (j / kBStages) & 1, &abort_flag, &g_bwd_status)))
+                return false;
             tc_fence_after();
             const uint64_t dK = d0 + static_cast<uint64_t>((s * kStageBytes) >> 4);
-            const uint64_t dV = d0 + static_cast<uint64_t>((s * kStageBytes + kTileBytes) >> 4);
-            const uint64_t dKv = d0 + static_cast<uint64_t>((s * kStageBytes + 2 * kTileBytes) >> 4);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kQKSteps; ++kk) {
                     // k-step kk: features [16 kk, 16 kk + 16) = 32 bytes of every token row
                     const int off = ((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128);
                     mma_f16_ts(tS, tQ + kk * 8, dK + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
-                    mma_f16_ts(tDP, tDO + kk * 8, dV + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(bars.sdp_full));
+                mma_commit(bar(bars.s_full));
             }
             __syncwarp();
+            return true;
+        };
+        auto issue_dp = [&](int j) {       // K/V of tile j landed (issue_s(j) waited for them)
+            const int s = j % kBStages;
+            const uint64_t dV = d0 + static_cast<uint64_t>((s * kStageBytes + kTileBytes) >> 4);
+            if (elect_one_sync()) {
+#pragma unroll
+                for (int kk = 0; kk < kQKSteps; ++kk) {
+                    const int off = ((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128);
+                    mma_f16_ts(tDP, tDO + kk * 8, dV + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(bars.dp_full));
+            }
+            __syncwarp();
+        };
+        // Issue order  S(0) dP(0) | S(1) dQ(0) dP(1) | S(2) dQ(1) dP(2) | ...:
+        // S(j + 1) runs while the dS warps work on tile j (they release the S
+        // columns as soon as S(j) is in their registers), and dS(j) goes over
+        // the front of dP(j)'s columns, which dP(j + 1) overwrites after dQ(j)
+        // has read them: the tensor core executes one thread's MMAs in issue
+        // order.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.qdo_full), 0, &abort_flag, &g_bwd_status));
+        if (ok && n_kv > 0) {
+            ok = issue_s(0);
+            if (ok) issue_dp(0);
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+            const int s = j % kBStages;
+            if (j + 1 < n_kv) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.s_free), j & 1, &abort_flag, &g_bwd_status)) ||
+                    !issue_s(j + 1)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.ds_full), j & 1, &abort_flag, &g_bwd_status))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const uint64_t dKv = d0 + static_cast<uint64_t>((s * kStageBytes + 2 * kTileBytes) >> 4);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kDQSteps; ++kk) {
                     // k-step kk: key columns [16 kk, 16 kk + 16); dS of key column
-                    // half h sits at the front of S columns [64 h, 64 h + 64)
-                    const uint32_t a = tS + (kk >> 2) * 64 + (kk & 3) * 8;
+                    // half h sits at the front of dP columns [64 h, 64 h + 64)
+                    const uint32_t a = tDP + (kk >> 2) * 64 + (kk & 3) * 8;
                     const int off = ((kk * 32) / 128) * (kD * 128) + ((kk * 32) % 128);
                     mma_f16_ts(tDQ, a, dKv + static_cast<uint64_t>(off >> 4), kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
                 }
@@ -251,6 +325,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
                 if (j == n_kv - 1) mma_commit(bar(bars.dq_final));
             }
             __syncwarp();
+            if (j + 1 < n_kv) issue_dp(j + 1);
         }
         if (!ok) {
             if (elect_one_sync()) {
@@ -314,51 +389,68 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         bool ok = true;
         int kc[3] = {box.k0[0], box.k0[1], box.k0[2]};
         for (int j = 0; j < n_kv && ok; ++j, bwd_odometer(kc, box)) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.sdp_full), j & 1, &abort_flag, &g_bwd_status));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full), j & 1, &abort_flag, &g_bwd_status));
             if (!ok) {
                 bwd_raise(&abort_flag);
                 break;
             }
             tc_fence_after();
+            // this half row of S(j), then its columns go back to the MMA warp for S(j + 1)
+            uint32_t rs[64];
+            tmem_ld32(tmem + kColS + lane_addr + half * 64, *reinterpret_cast<uint32_t(*)[32]>(rs));
+            tmem_ld32(tmem + kColS + lane_addr + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars.s_free));
+            bwd_reg_fence(rs);
             bool full = true;
 #pragma unroll
             for (int d = 0; d < 3; ++d) full = full && kc[d] >= box.full_lo[d] && kc[d] <= box.full_hi[d];
-            // two pieces of 32 key columns: S, dP -> dS (bf16) over the front of this half's S columns
+            // this row's window relative to the KV tile's origin, per dimension
+            const int lo_t = st[0] - kc[0] * p.tile[0];
+            const int lo_y = st[1] - kc[1] * p.tile[1];
+            const int lo_x = st[2] - kc[2] * p.tile[2];
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.dp_full), j & 1, &abort_flag, &g_bwd_status));
+            if (!ok) {
+                bwd_raise(&abort_flag);
+                break;
+            }
+            tc_fence_after();
+            // two pieces of 32 key columns: S, dP -> dS (bf16) over the front of this half's dP columns
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc) {
-                uint32_t rs[32], rp[32];
+                uint32_t rp[32];
                 const uint32_t col = half * 64 + pc * 32;
-                tmem_ld32(tmem + kColS + lane_addr + col, rs);
                 tmem_ld32(tmem + kColDP + lane_addr + col, rp);
+                // key column c of the piece is inside the window iff bit c is set
+                // (all set on a tile that lies in every window of the Q tile)
+                const uint32_t m = !row_valid ? 0u
+                                   : full     ? 0xffffffffu
+                                              : box_mask_word(static_cast<int>(col) >> 5, p.tlog[0], p.tlog[1],
+                                                              p.tlog[2], lo_t, lo_y, lo_x, p.win[0], p.win[1], p.win[2]);
                 tmem_wait_ld();
-                bwd_reg_fence(rs);
                 bwd_reg_fence(rp);
+                const float2 sc2 = make_float2(scale_log2, scale_log2);
+                const float2 nl2 = make_float2(-lse2, -lse2);
+                const float2 nd2 = make_float2(-delta, -delta);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    float ds2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int c = 2 * i + e;
-                        bool valid = row_valid;
-                        if (!full) {
-                            // key (t, y, x) of column col + c inside this KV tile
-                            const int kcol = static_cast<int>(col) + c;
-                            const int cx = kcol & (p.tile[2] - 1);
-                            const int cy = (kcol >> p.tlog[2]) & (p.tile[1] - 1);
-                            const int ct = kcol >> (p.tlog[1] + p.tlog[2]);
-                            valid = valid &&
-                                    static_cast<unsigned>(kc[0] * p.tile[0] + ct - st[0]) < static_cast<unsigned>(p.win[0]) &&
-                                    static_cast<unsigned>(kc[1] * p.tile[1] + cy - st[1]) < static_cast<unsigned>(p.win[1]) &&
-                                    static_cast<unsigned>(kc[2] * p.tile[2] + cx - st[2]) < static_cast<unsigned>(p.win[2]);
-                        }
-                        const float pr = valid ? bwd_exp2(__uint_as_float(rs[c]) * scale_log2 - lse2) : 0.0f;
-                        ds2[e] = pr * (__uint_as_float(rp[c]) - delta);
-                    }
-                    __nv_bfloat162 h = __floats2bfloat162_rn(ds2[0], ds2[1]);
+                    const int c = 2 * i;
+                    // p = exp2(s scale log2(e) - lse log2(e)), 0 outside the window
+                    const float s0 = (m >> c) & 1u ? __uint_as_float(rs[pc * 32 + c]) : -INFINITY;
+                    const float s1 = (m >> (c + 1)) & 1u ? __uint_as_float(rs[pc * 32 + c + 1]) : -INFINITY;
+                    const float2 x = bwd_ffma2(make_float2(s0, s1), sc2, nl2);
+                    const float2 pr = make_float2(bwd_exp2(x.x), bwd_exp2(x.y));
+                    // dS = p (dP - delta)
+                    const float2 dd = bwd_fadd2(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), nd2);
+                    const float2 ds2 = bwd_fmul2(pr, dd);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(ds2.x, ds2.y);
                     pk[i] = *reinterpret_cast<uint32_t*>(&h);
                 }
-                tmem_st16(tmem + kColS + lane_addr + half * 64 + pc * 16, pk);
+                // dS of these 32 keys over dP columns this thread already read
+                tmem_st16(tmem + kColDP + lane_addr + half * 64 + pc * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -412,12 +504,14 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
 //   S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T            (A, B from shared memory)
 //   P^T  = exp(S^T - lse_i),  dS^T = P^T (dP^T - delta_i)   (per key row)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i               (A from TMEM, B MN-major)
-// TMEM: dV [0, 128), dK [128, 256), S^T [256, 384), dP^T [384, 512); each
-// thread half writes its P^T / dS^T columns over the front of its own S^T /
-// dP^T columns.  Q_i and dO_i are read as tiled tiles in both roles: K-major
-// for S^T and dP^T, MN-major (token rows, 16 per k-step) for dV and dK.
-// The element mask comes from, per dimension, the interval of query
-// positions whose window holds this thread's key; a key row whose interval
+// TMEM: dV [0, 128), dK [128, 256), S^T [256, 384), dP^T [384, 512); P^T and
+// dS^T of each 32-query piece go over that piece's own dP^T columns (16 + 16),
+// so S^T is free once it is in registers and S^T of the next Q tile is
+// computed while the key-row warps work.  Q_i and dO_i are read as tiled tiles
+// in both roles: K-major for S^T and dP^T, MN-major (token rows, 16 per
+// k-step) for dV and dK.  The element mask comes from, per dimension, the
+// interval of query positions whose window holds this thread's key (one
+// 32-bit word per 32 query columns, box_mask_word); a key row whose interval
 // covers the whole Q tile needs no mask.
 
 constexpr uint32_t kColDV = 0;
@@ -432,8 +526,10 @@ struct KVBars {
     uint64_t kv_full;             // K_j and V_j landed
     uint64_t full[kBStages];      // Q_i, dO_i, lse_i, delta_i landed
     uint64_t empty[kBStages];     // the four MMAs of step i are done
-    uint64_t sdp_full;            // S^T and dP^T of step i are in TMEM
-    uint64_t p_full;              // P^T and dS^T of step i are in TMEM (8 warps)
+    uint64_t s_full;              // S^T of step i is in TMEM (one phase per step)
+    uint64_t s_free;              // the key-row warps hold S^T(i) in registers (8 warps)
+    uint64_t dp_full;             // dP^T of step i is in TMEM
+    uint64_t p_full;              // P^T and dS^T of step i are in TMEM, over dP^T (8 warps)
     uint64_t final_;              // the last dV / dK products are done
     uint64_t drain;
 };
@@ -486,7 +582,9 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             mbar_init(bar(bars.full[s]), 1);
             mbar_init(bar(bars.empty[s]), 1);
         }
-        mbar_init(bar(bars.sdp_full), 1);
+        mbar_init(bar(bars.s_full), 1);
+        mbar_init(bar(bars.s_free), kBSoftmaxWarps);
+        mbar_init(bar(bars.dp_full), 1);
         mbar_init(bar(bars.p_full), kBSoftmaxWarps);
         mbar_init(bar(bars.final_), 1);
         mbar_init(bar(bars.drain), 1);
@@ -558,48 +656,83 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         const uint32_t tDV = tmem + kColDV, tDK = tmem + kColDK, tST = tmem + kColST, tDPT = tmem + kColDPT;
         const uint64_t dKj = make_smem_desc(sK, 16, 8 * 128, kSwizzle128B);
         const uint64_t dVj = make_smem_desc(sV, 16, 8 * 128, kSwizzle128B);
-        bool ok = n_q == 0 || __all_sync(0xffffffffu, mbar_wait(bar(bars.kv_full), 0, &abort_flag, &g_bwd_status));
-        for (int i = 0; ok && i < n_q; ++i) {
+        auto stage_of = [&](int i) { return sStage + (i % kBStages) * kKVStageBytes; };
+        // S^T(i) = K_j Q_i^T (both operands from shared memory)
+        auto issue_s = [&](int i) -> bool {
             const int s = i % kBStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag, &g_bwd_status))) {
-                ok = false;
-                break;
-            }
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag, &g_bwd_status)))
+                return false;
             tc_fence_after();
-            const uint32_t st = sStage + s * kKVStageBytes;
-            const uint64_t dQk = make_smem_desc(st, 16, 8 * 128, kSwizzle128B);                // K-major
-            const uint64_t dDOk = make_smem_desc(st + kTileBytes, 16, 8 * 128, kSwizzle128B);
-            const uint64_t dQm = make_smem_desc(st, kTileElems * 128, 8 * 128, kSwizzle128B);   // MN-major
-            const uint64_t dDOm = make_smem_desc(st + kTileBytes, kTileElems * 128, 8 * 128, kSwizzle128B);
+            const uint64_t dQk = make_smem_desc(stage_of(i), 16, 8 * 128, kSwizzle128B);   // K-major
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kQKSteps; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128)) >> 4);
                     mma_f16_ss(tST, dKj + off, dQk + off, kIdesc, kk > 0 ? 1u : 0u);
-                    mma_f16_ss(tDPT, dVj + off, dDOk + off, kIdesc, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(bars.sdp_full));
+                mma_commit(bar(bars.s_full));
             }
             __syncwarp();
+            return true;
+        };
+        // dP^T(i) = V_j dO_i^T (step i's stage has landed: issue_s(i) waited for it)
+        auto issue_dp = [&](int i) {
+            const uint64_t dDOk = make_smem_desc(stage_of(i) + kTileBytes, 16, 8 * 128, kSwizzle128B);
+            if (elect_one_sync()) {
+#pragma unroll
+                for (int kk = 0; kk < kQKSteps; ++kk) {
+                    const uint64_t off = static_cast<uint64_t>((((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128)) >> 4);
+                    mma_f16_ss(tDPT, dVj + off, dDOk + off, kIdesc, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(bar(bars.dp_full));
+            }
+            __syncwarp();
+        };
+        // Issue order  S^T(0) dP^T(0) | S^T(1) dV(0) dK(0) dP^T(1) | ...: S^T(i + 1)
+        // runs while the key-row warps work on step i (they release the S^T
+        // columns once S^T(i) is in their registers); P^T(i) and dS^T(i) go over
+        // dP^T(i)'s columns, which dP^T(i + 1) overwrites after dV(i) and dK(i)
+        // have read them: the tensor core executes one thread's MMAs in issue
+        // order.
+        bool ok = n_q == 0 || __all_sync(0xffffffffu, mbar_wait(bar(bars.kv_full), 0, &abort_flag, &g_bwd_status));
+        if (ok && n_q > 0) {
+            ok = issue_s(0);
+            if (ok) issue_dp(0);
+        }
+        for (int i = 0; ok && i < n_q; ++i) {
+            const int s = i % kBStages;
+            if (i + 1 < n_q) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.s_free), i & 1, &abort_flag, &g_bwd_status)) ||
+                    !issue_s(i + 1)) {
+                    ok = false;
+                    break;
+                }
+            }
             if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.p_full), i & 1, &abort_flag, &g_bwd_status))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const uint32_t st = stage_of(i);
+            const uint64_t dQm = make_smem_desc(st, kTileElems * 128, 8 * 128, kSwizzle128B);   // MN-major
+            const uint64_t dDOm = make_smem_desc(st + kTileBytes, kTileElems * 128, 8 * 128, kSwizzle128B);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kDQSteps; ++kk) {
-                    // k-step kk: query columns [16 kk, 16 kk + 16) = token rows of Q_i / dO_i
-                    const uint32_t a = (kk >> 2) * 64 + (kk & 3) * 8;
+                    // k-step kk: query columns [16 kk, 16 kk + 16) = token rows of Q_i / dO_i.
+                    // Query piece c (32 columns) keeps P^T at dP^T columns [32 c, 32 c + 16)
+                    // and dS^T at [32 c + 16, 32 c + 32)
+                    const uint32_t a = (kk >> 1) * 32 + (kk & 1) * 8;
                     const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
                     const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    mma_f16_ts(tDV, tST + a, dDOm + off, kIdescMN, acc);
-                    mma_f16_ts(tDK, tDPT + a, dQm + off, kIdescMN, acc);
+                    mma_f16_ts(tDV, tDPT + a, dDOm + off, kIdescMN, acc);
+                    mma_f16_ts(tDK, tDPT + a + 16, dQm + off, kIdescMN, acc);
                 }
                 mma_commit(bar(bars.empty[s]));
                 if (i == n_q - 1) mma_commit(bar(bars.final_));
             }
             __syncwarp();
+            if (i + 1 < n_q) issue_dp(i + 1);
         }
         if (!ok) {
             if (elect_one_sync()) {
@@ -646,68 +779,84 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         for (int i = 0; i < n_q && ok; ++i, bwd_odometer(qc, qbox)) {
             const int s = i % kBStages;
             ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag, &g_bwd_status)) &&
-                 __all_sync(0xffffffffu, mbar_wait(bar(bars.sdp_full), i & 1, &abort_flag, &g_bwd_status));
+                 __all_sync(0xffffffffu, mbar_wait(bar(bars.s_full), i & 1, &abort_flag, &g_bwd_status));
             if (!ok) {
                 bwd_raise(&abort_flag);
                 break;
             }
             tc_fence_after();
-            // query window of this key in the Q tile's own coordinates
-            int lo[3], span[3];
+            // this half row of S^T(i); then its columns go back for S^T(i + 1)
+            uint32_t rs[64];
+            tmem_ld32(tmem + kColST + lane_addr + half * 64, *reinterpret_cast<uint32_t(*)[32]>(rs));
+            tmem_ld32(tmem + kColST + lane_addr + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars.s_free));
+            bwd_reg_fence(rs);
+            // the queries whose window holds this key, in the Q tile's own
+            // coordinates: [lo_d, lo_d + len_d) per dimension
+            int lo[3], len[3];
             bool full = true;
 #pragma unroll
             for (int d = 0; d < 3; ++d) {
                 lo[d] = qlo[d] - qc[d] * p.tile[d];
-                span[d] = qhi[d] - qlo[d];                         // negative: empty
-                full = full && lo[d] <= 0 && qhi[d] - qc[d] * p.tile[d] >= p.tile[d] - 1;
+                len[d] = qhi[d] - qlo[d] + 1;                      // <= 0: empty
+                full = full && len[d] > 0 && lo[d] <= 0 && lo[d] + len[d] >= p.tile[d];
             }
             const float* lse_s = stage_f + s * (kKVStageBytes / 4) + 2 * (kTileBytes / 4);
             const float* delta_s = lse_s + kTileElems;
+            const float2 sc2 = make_float2(scale_log2, scale_log2);
+            const float2 nlog2e = make_float2(-kBLog2e, -kBLog2e);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.dp_full), i & 1, &abort_flag, &g_bwd_status));
+            if (!ok) {
+                bwd_raise(&abort_flag);
+                break;
+            }
+            tc_fence_after();
+            // two pieces of 32 query columns; P^T and dS^T of a piece (16 columns
+            // each) go over the piece's own dP^T columns, which are read first
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc) {
-                uint32_t rs[32], rp[32];
                 const int col0 = half * 64 + pc * 32;
-                tmem_ld32(tmem + kColST + lane_addr + col0, rs);
+                const uint32_t* rsp = rs + pc * 32;
+                uint32_t rp[32];
                 tmem_ld32(tmem + kColDPT + lane_addr + col0, rp);
+                // query column c of the piece reaches this key iff bit c is set
+                const uint32_t m = full ? 0xffffffffu
+                                        : box_mask_word(col0 >> 5, p.tlog[0], p.tlog[1], p.tlog[2], lo[0], lo[1], lo[2],
+                                                        len[0], len[1], len[2]);
                 tmem_wait_ld();
-                bwd_reg_fence(rs);
                 bwd_reg_fence(rp);
                 uint32_t pkp[16], pkd[16];
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
                     const float4 L4 = *reinterpret_cast<const float4*>(lse_s + col0 + 4 * g4);
                     const float4 D4 = *reinterpret_cast<const float4*>(delta_s + col0 + 4 * g4);
-                    const float Lv[4] = {L4.x, L4.y, L4.z, L4.w};
-                    const float Dv[4] = {D4.x, D4.y, D4.z, D4.w};
-                    float pv[4], dsv[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int c = col0 + 4 * g4 + e;               // query column of the Q tile
-                        bool valid = full;
-                        if (!full) {
-                            const int cx = c & (p.tile[2] - 1);
-                            const int cy = (c >> p.tlog[2]) & (p.tile[1] - 1);
-                            const int ct = c >> (p.tlog[1] + p.tlog[2]);
-                            valid = static_cast<unsigned>(ct - lo[0]) <= static_cast<unsigned>(span[0]) &&
-                                    static_cast<unsigned>(cy - lo[1]) <= static_cast<unsigned>(span[1]) &&
-                                    static_cast<unsigned>(cx - lo[2]) <= static_cast<unsigned>(span[2]) &&
-                                    span[0] >= 0 && span[1] >= 0 && span[2] >= 0;
-                        }
-                        const int k = 4 * g4 + e;
-                        pv[e] = valid ? bwd_exp2(__uint_as_float(rs[k]) * scale_log2 - Lv[e] * kBLog2e) : 0.0f;
-                        dsv[e] = pv[e] * (__uint_as_float(rp[k]) - Dv[e]);
+                    for (int e = 0; e < 4; e += 2) {
+                        const int k = 4 * g4 + e;                      // column of the piece
+                        // p = exp2(s scale log2(e) - lse log2(e)), 0 where the query does not
+                        // reach the key (selected after the exponential: a padding query's
+                        // lse is -inf, so its exponent may be anything there)
+                        const float2 lse2 = e == 0 ? make_float2(L4.x, L4.y) : make_float2(L4.z, L4.w);
+                        const float2 dl2 = e == 0 ? make_float2(D4.x, D4.y) : make_float2(D4.z, D4.w);
+                        const float2 x = bwd_ffma2(make_float2(__uint_as_float(rsp[k]), __uint_as_float(rsp[k + 1])), sc2,
+                                                   bwd_fmul2(lse2, nlog2e));
+                        const float2 pr = make_float2((m >> k) & 1u ? bwd_exp2(x.x) : 0.0f,
+                                                      (m >> (k + 1)) & 1u ? bwd_exp2(x.y) : 0.0f);
+                        // dS = p (dP - delta)
+                        const float2 dd = bwd_fadd2(make_float2(__uint_as_float(rp[k]), __uint_as_float(rp[k + 1])),
+                                                    make_float2(-dl2.x, -dl2.y));
+                        const float2 ds2 = bwd_fmul2(pr, dd);
+                        __nv_bfloat162 hp = __floats2bfloat162_rn(pr.x, pr.y);
+                        __nv_bfloat162 hd = __floats2bfloat162_rn(ds2.x, ds2.y);
+                        pkp[k / 2] = *reinterpret_cast<uint32_t*>(&hp);
+                        pkd[k / 2] = *reinterpret_cast<uint32_t*>(&hd);
                     }
-                    __nv_bfloat162 h0 = __floats2bfloat162_rn(pv[0], pv[1]);
-                    __nv_bfloat162 h1 = __floats2bfloat162_rn(pv[2], pv[3]);
-                    __nv_bfloat162 g0 = __floats2bfloat162_rn(dsv[0], dsv[1]);
-                    __nv_bfloat162 g1 = __floats2bfloat162_rn(dsv[2], dsv[3]);
-                    pkp[2 * g4] = *reinterpret_cast<uint32_t*>(&h0);
-                    pkp[2 * g4 + 1] = *reinterpret_cast<uint32_t*>(&h1);
-                    pkd[2 * g4] = *reinterpret_cast<uint32_t*>(&g0);
-                    pkd[2 * g4 + 1] = *reinterpret_cast<uint32_t*>(&g1);
                 }
-                tmem_st16(tmem + kColST + lane_addr + half * 64 + pc * 16, pkp);
-                tmem_st16(tmem + kColDPT + lane_addr + half * 64 + pc * 16, pkd);
+                tmem_st16(tmem + kColDPT + lane_addr + col0, pkp);
+                tmem_st16(tmem + kColDPT + lane_addr + col0 + 16, pkd);
             }
             tmem_wait_st();
             tc_fence_before();

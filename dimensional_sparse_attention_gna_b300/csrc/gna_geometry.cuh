@@ -77,4 +77,40 @@ __host__ __device__ __forceinline__ void dim_full_range(int t, int L, int w, con
     hi = end >= 0 ? end / t : -1;
 }
 
+// Bit c of the result is set iff element 32 * wi + c of a tile lies inside a
+// box: the tile has 2^tl[d] elements per dimension, stored in (t, y, x) order,
+// and the box holds the element coordinates with 0 <= c_d - lo_d < len_d in
+// every dimension (len_d <= 0: empty).  One word covers 32 consecutive
+// elements, i.e. one or more whole x rows of the tile, or part of one.
+__host__ __device__ __forceinline__ uint32_t box_mask_word(int wi, int tl_t, int tl_y, int tl_x, int lo_t, int lo_y,
+                                                           int lo_x, int len_t, int len_y, int len_x)
+{
+    auto in = [](int c, int lo, int len) { return static_cast<unsigned>(c - lo) < static_cast<unsigned>(len); };
+    auto bits = [](int a, int b) -> uint32_t {   // bits [a, b) clipped to [0, 32)
+        a = a < 0 ? 0 : a;
+        b = b > 32 ? 32 : b;
+        if (b <= a) return 0u;
+        return ((b - a) >= 32 ? 0xffffffffu : ((1u << (b - a)) - 1u)) << a;
+    };
+    if (len_t <= 0 || len_y <= 0 || len_x <= 0) return 0u;
+    const int tw = 1 << tl_x;
+    if (tl_x >= 5) {
+        // the word is part of one x row: group (t, y) of element 32 wi
+        const int e0 = wi * 32;
+        const int g = e0 >> tl_x;
+        const int cy = g & ((1 << tl_y) - 1), ct = g >> tl_y;
+        if (!in(ct, lo_t, len_t) || !in(cy, lo_y, len_y)) return 0u;
+        const int bx = e0 & (tw - 1);
+        return bits(lo_x - bx, lo_x - bx + len_x);
+    }
+    const uint32_t xrow = bits(lo_x, lo_x + len_x) & ((1u << tw) - 1u);
+    uint32_t w = 0u;
+    for (int gi = 0; gi < (32 >> tl_x); ++gi) {
+        const int g = ((wi * 32) >> tl_x) + gi;
+        const int cy = g & ((1 << tl_y) - 1), ct = g >> tl_y;
+        if (in(ct, lo_t, len_t) && in(cy, lo_y, len_y)) w |= xrow << (gi * tw);
+    }
+    return w;
+}
+
 }  // namespace gna
