@@ -5,7 +5,8 @@ One step = one pass of the whole path over one batch of synthetic input:
     ->  fused GNA forward
     ->  unpermute O and lse (tiles -> raster)
 or, with ``--layout raster``, permute V -> the forward reading Q, K and
-writing O, lse in the raster layout, on the 720p-video latent workload (30 x 48 x 80 tokens, 24 heads, head_dim 128,
+writing O, lse in the raster layout, or with ``--layout raster_all`` the forward
+alone on every tensor in the raster layout (no permute), on the 720p-video latent workload (30 x 48 x 80 tokens, 24 heads, head_dim 128,
 window 16 x 32 x 48, bf16), the configuration the GNA page's video results and
 its Blackwell kernel throughput are about.
 
@@ -56,9 +57,10 @@ def parse_args(argv=None):
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--head-dim", type=int, default=128)
     ap.add_argument("--dtype", default="bf16", choices=["bf16", "fp8"])
-    ap.add_argument("--layout", default="tiled", choices=["tiled", "raster"],
+    ap.add_argument("--layout", default="tiled", choices=["tiled", "raster", "raster_all"],
                     help="tiled: permute Q, K, V and unpermute O, lse around gna_forward; "
-                         "raster: permute V only, gna_forward_raster on raster Q, K, O, lse")
+                         "raster: permute V only, gna_forward_raster on raster Q, K, O, lse; "
+                         "raster_all: no permute, gna_forward_raster_all on raster Q, K, V, O, lse (bf16, d 128)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--sustain", type=float, default=0.0,
@@ -381,19 +383,24 @@ def gpu_arm(a, rank, world, local):
             descale = (descale or []) + [s]
         del x
     ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)
-    raster = a.layout == "raster"
+    raster = a.layout in ("raster", "raster_all")
+    raster_v = a.layout == "raster_all"
     shp = G.tiled_shape(B, heads, dims, d)
     if not raster:                      # the raster path has no tiled Q, K, O or lse
         qt, kt = (torch.empty(shp, dtype=dt, device=dev) for _ in range(2))
         out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
         lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
-    vt = torch.empty(G.value_shape(B, heads, dims, d), dtype=dt, device=dev)
+    if not raster_v:                    # the all-raster path reads V as it is
+        vt = torch.empty(G.value_shape(B, heads, dims, d), dtype=dt, device=dev)
     out = torch.empty(raster_shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(raster_shape[:-1] + (1,), dtype=torch.float32, device=dev)
 
-    def forward(window, stride, q_in, k_in, o_dst, lse_dst):
+    def forward(window, stride, q_in, k_in, o_dst, lse_dst, v_in=None):
         """One forward launch of the bench's layout (raster tensors in, raster out)."""
-        if raster:
+        if raster_v:
+            G.gna_forward_raster_all(q_in, k_in, xs[2] if v_in is None else v_in, o_dst, lse_dst[..., 0], B, heads,
+                                     dims, window, stride, d, stream=stream)
+        elif raster:
             G.gna_forward_raster(q_in, k_in, vt, o_dst, lse_dst[..., 0], B, heads, dims, window, stride, d,
                                  descale=ds, stream=stream)
         else:
@@ -403,7 +410,8 @@ def gpu_arm(a, rank, world, local):
         if not raster:
             G.gna_permute(q_in, qt, B, heads, dims, d, stream=stream)
             G.gna_permute(k_in, kt, B, heads, dims, d, stream=stream)
-        G.gna_permute_v(v_in, vt, B, heads, dims, d, stream=stream)
+        if not raster_v:
+            G.gna_permute_v(v_in, vt, B, heads, dims, d, stream=stream)
 
     def unpermute_out(o_dst, lse_dst):
         if not raster:
@@ -428,7 +436,7 @@ def gpu_arm(a, rank, world, local):
             ev["perm"].append((e[0], e[1]))
             ev["fwd"].append((e[1], e[2]))
             ev["unperm"].append((e[2], e[3]))
-    launches_per_step = 2 if raster else 6
+    launches_per_step = 1 if raster_v else 2 if raster else 6
 
     for _ in range(a.warmup):
         step()
@@ -462,7 +470,7 @@ def gpu_arm(a, rank, world, local):
     value = total_flops / (elapsed_ms / 1e3) / 1e12
     kernel_tflops = flops_rank / (fwd_ms / 1e3) / 1e12
     esz = torch.tensor([], dtype=dt).element_size()
-    perm_bytes = (1 if raster else 3) * 2 * B * math.prod(dims) * heads * d * esz
+    perm_bytes = (0 if raster_v else 1 if raster else 3) * 2 * B * math.prod(dims) * heads * d * esz
     unperm_bytes = 0 if raster else 2 * B * math.prod(dims) * heads * (d * 2 + 4)
 
     peaks, peaks_kind = load_peaks()
@@ -539,7 +547,7 @@ def gpu_arm(a, rank, world, local):
                 ev["perm_done"][b].record(stream)
             if used["out_done"][b]:
                 stream.wait_event(ev["out_done"][b])      # results of step k-2 downloaded
-            forward(a.window, a.stride, dev_in[b][0], dev_in[b][1], dev_out[b], dev_lse[b])
+            forward(a.window, a.stride, dev_in[b][0], dev_in[b][1], dev_out[b], dev_lse[b], dev_in[b][2])
             if raster:
                 ev["perm_done"][b].record(stream)         # the forward read the raster Q, K
             used["perm_done"][b] = True
@@ -667,10 +675,10 @@ def gpu_arm(a, rank, world, local):
                      "frac_of_sustained_peak": kernel_tflops / peak_sustained,
                      "tile_work_tflops": tile_flops / (fwd_ms / 1e3) / 1e12,
                      "tile_overhead": tile_flops / flops_rank, "partial_tile_share": partial / visited},
-        "kernels_ms": {("permute_v" if raster else "permute_qkv"): perm_ms, "forward": fwd_ms,
+        "kernels_ms": {("permute_v" if raster else "permute_qkv"): None if raster_v else perm_ms, "forward": fwd_ms,
                        "unpermute_o_lse": None if raster else unperm_ms},
-        "permute_gbps": perm_bytes / (perm_ms / 1e3) / 1e9,
-        "permute_frac_of_hbm": perm_bytes / (perm_ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6400.0),
+        "permute_gbps": None if raster_v else perm_bytes / (perm_ms / 1e3) / 1e9,
+        "permute_frac_of_hbm": None if raster_v else perm_bytes / (perm_ms / 1e3) / 1e9 / peaks.get("hbm_gbs", 6400.0),
         "unpermute_gbps": None if raster else unperm_bytes / (unperm_ms / 1e3) / 1e9,
         "dense_forward_ms": dense_ms, "speedup_vs_dense": speedup,
         "dense_clocks": dense_clk, "speedup_vs_dense_clock_normalised": speedup_clock_normalised,

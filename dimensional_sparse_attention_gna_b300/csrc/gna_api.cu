@@ -456,9 +456,10 @@ gna_status gna_plan_tile(const int dims[3], const int window[3], const int strid
 
 namespace {
 
+// raster: 0 = tiled q, k, out, lse; 1 = raster q, k, out, lse; 2 = raster v as well
 gna_status forward_impl(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
                         const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
-                        const gna_options* opt, void* stream, bool raster)
+                        const gna_options* opt, void* stream, int raster)
 {
     if (q == nullptr || k == nullptr || v == nullptr || out == nullptr)
         return fail(GNA_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -471,6 +472,9 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
     if (es == 0) return fail(GNA_ERR_INVALID_ARG, "forward dtype must be GNA_BF16 or GNA_FP8_E4M3");
     if (!((es == 2 && (head_dim == 32 || head_dim == 64 || head_dim == 128)) || (es == 1 && head_dim == 128)))
         return fail(GNA_ERR_UNSUPPORTED, "head_dim %d is not supported for this dtype", head_dim);
+    if (raster == 2 && !(es == 2 && head_dim == 128))
+        return fail(GNA_ERR_UNSUPPORTED, "raster v: bf16 with head_dim 128 only (use gna_forward_raster with v in the "
+                                         "value layout)");
     const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
     if (rule != GNA_LEADER_CENTER && rule != GNA_LEADER_LITERAL)
         return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", rule);
@@ -509,7 +513,7 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
     p.fault_skip_kv = g_skip_kv_forward.load(std::memory_order_relaxed);
 
     p.q = q;
-    p.raster = raster ? 1 : 0;
+    p.raster = raster;
     if (raster) {
         if (static_cast<int64_t>(B) * dims[0] > INT32_MAX || static_cast<int64_t>(heads) * head_dim > INT32_MAX)
             return fail(GNA_ERR_UNSUPPORTED, "raster tensor too large for TMA coordinates");
@@ -517,7 +521,11 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
     } else if ((st = make_tile_map(&p.tmK, k, rows, head_dim, es)) != GNA_OK) {
         return st;
     }
-    if ((st = make_value_map(&p.tmV, v, num_q_tiles, head_dim, es)) != GNA_OK) return st;
+    if (raster == 2) {
+        if ((st = make_raster_map(&p.tmV, v, B, dims, heads, head_dim, es, p.tile)) != GNA_OK) return st;
+    } else if ((st = make_value_map(&p.tmV, v, num_q_tiles, head_dim, es)) != GNA_OK) {
+        return st;
+    }
 
     cudaError_t e = gna::launch_forward(p, head_dim, es, num_q_tiles, static_cast<cudaStream_t>(stream));
     if (e == cudaErrorNotSupported) return fail(GNA_ERR_UNSUPPORTED, "no kernel for head_dim %d", head_dim);
@@ -532,7 +540,7 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v, void* out
                           const int dims[3], const int window[3], const int stride[3], int head_dim, gna_dtype dtype,
                           const gna_options* opt, void* stream)
 {
-    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, false);
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, 0);
 }
 
 gna_status gna_forward(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
@@ -542,7 +550,7 @@ gna_status gna_forward(const void* q, const void* k, const void* v, void* out, f
     if (dtype == GNA_FP8_E4M3)
         return fail(GNA_ERR_INVALID_ARG, "gna_forward takes GNA_BF16; e4m3 codes need their descales: "
                                          "call gna_forward_fp8");
-    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, nullptr, stream, false);
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, nullptr, stream, 0);
 }
 
 gna_status gna_forward_fp8(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
@@ -553,14 +561,21 @@ gna_status gna_forward_fp8(const void* q, const void* k, const void* v, void* ou
     gna_options opt{};
     opt.descale = descale_qkv;
     return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, GNA_FP8_E4M3, &opt, stream,
-                        false);
+                        0);
 }
 
 gna_status gna_forward_raster(const void* q, const void* k, const void* v, void* out, float* lse, int B, int heads,
                               const int dims[3], const int window[3], const int stride[3], int head_dim,
                               gna_dtype dtype, const gna_options* opt, void* stream)
 {
-    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, true);
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, 1);
+}
+
+gna_status gna_forward_raster_all(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                  int heads, const int dims[3], const int window[3], const int stride[3],
+                                  int head_dim, gna_dtype dtype, const gna_options* opt, void* stream)
+{
+    return forward_impl(q, k, v, out, lse, B, heads, dims, window, stride, head_dim, dtype, opt, stream, 2);
 }
 
 gna_status gna_schedule_step(int step, int num_steps, int full_steps, const int dims[3], const int window[3],

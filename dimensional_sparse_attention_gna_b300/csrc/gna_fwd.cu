@@ -112,6 +112,8 @@ struct Cfg {
     static constexpr int kPVSteps = kTileElems / kKPerInstr;
     static constexpr uint32_t kIdescQK = make_idesc(128, 128, Precision<ESZ>::fmt, false);
     static constexpr uint32_t kIdescPV = make_idesc(128, D, Precision<ESZ>::fmt, false);
+    // raster V (RASTER_V): the tile lands token-major like K, the MN-major B of P V
+    static constexpr uint32_t kIdescPVmn = make_idesc(128, D, Precision<ESZ>::fmt, true);
     // V arrives in the value layout: a d x 128 (feature-major) tile, loaded as
     // ESZ boxes of d rows x 128 bytes, which is the K-major B operand of P V
     static constexpr int kVChunks = ESZ;
@@ -323,10 +325,13 @@ __device__ __forceinline__ void rescale_o(uint32_t taddr, float alpha)
 }
 
 // TT, TH, TW: the layout tile when known at compile time (the default tiles),
-// or 0, 0, 0 for any tile (runtime shape, slower mask construction).
-template <int D, int ESZ, int NS, int TT, int TH, int TW, bool RASTER>
+// or 0, 0, 0 for any tile (runtime shape, slower mask construction).  RASTER:
+// q, k, out and lse in the raster layout; RASTER_V: v too (bf16, head_dim 128),
+// loaded like k and read by P V as an MN-major operand.
+template <int D, int ESZ, int NS, int TT, int TH, int TW, bool RASTER, bool RASTER_V>
 __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_constant__ FwdParams p)
 {
+    static_assert(!RASTER_V || (RASTER && ESZ == 2 && D == 128), "raster V: bf16, head_dim 128, raster q and k");
     using C = Cfg<D, ESZ, NS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -436,11 +441,20 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
             }
             if (elect_one_sync()) {
                 mbar_arrive_expect_tx(bar(bars.v_full[s]), C::kTileBytes);
-                const int32_t vrow = static_cast<int32_t>((kv_row_base / kTileElems + tile_id) * D);
+                if constexpr (RASTER_V) {
+                    // token-major, exactly as the K tile (positions past the grid read as zero)
 #pragma unroll
-                for (int c = 0; c < C::kVChunks; ++c)
-                    tma_load_2d(sV + s * C::kTileBytes + c * C::kVChunkBytes, &p.tmV, bar(bars.v_full[s]),
-                                c * C::kVChunkElems, vrow);
+                    for (int c = 0; c < C::kChunks; ++c)
+                        tma_load_5d(sV + s * C::kTileBytes + c * kTileElems * C::kRowBytes, &p.tmV, bar(bars.v_full[s]),
+                                    h_idx * D + c * C::kChunkElems, kc[2] * p.tile[2], kc[1] * p.tile[1],
+                                    kc[0] * p.tile[0], b_idx);
+                } else {
+                    const int32_t vrow = static_cast<int32_t>((kv_row_base / kTileElems + tile_id) * D);
+#pragma unroll
+                    for (int c = 0; c < C::kVChunks; ++c)
+                        tma_load_2d(sV + s * C::kTileBytes + c * C::kVChunkBytes, &p.tmV, bar(bars.v_full[s]),
+                                    c * C::kVChunkElems, vrow);
+                }
             }
             __syncwarp();
             ++v_issued;
@@ -462,7 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         // descriptors of stage 0, chunk 0; stage / k-step offsets are added
         // to the start-address field (addresses >> 4 stay below 2^14)
         const uint64_t dK0 = make_smem_desc(sK, 16, 8 * C::kRowBytes, C::kSwizzle);
-        const uint64_t dV0 = make_smem_desc(sV, 16, 1024, kSwizzle128B);
+        // value layout: K-major (feature rows of 128 tokens); raster V: MN-major (token
+        // rows, the next 64 features 16 KB on, 8-token groups 1 KB apart)
+        const uint64_t dV0 = RASTER_V ? make_smem_desc(sV, kTileElems * C::kRowBytes, 8 * C::kRowBytes, kSwizzle128B)
+                                      : make_smem_desc(sV, 16, 1024, kSwizzle128B);
         auto issue_pv = [&](int i) -> bool {
             const int s = i % NS;
             if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.v_full[s]), (i / NS) & 1, &abort_flag, &g_device_status))) return false;
@@ -473,11 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
                 const uint32_t tP = tmem + p_col<ESZ>(i & 1);
 #pragma unroll
                 for (int kk = 0; kk < C::kPVSteps; ++kk) {
-                    // k-step kk covers tokens [kk * K, kk * K + K): 32 bytes of every feature row
-                    const int off = ((kk * 32) / 128) * C::kVChunkBytes + ((kk * 32) % 128);
+                    // k-step kk covers tokens [kk * K, kk * K + K): 32 bytes of every feature
+                    // row (value layout), or K token rows (raster V)
+                    const int off = RASTER_V ? kk * C::kKPerInstr * C::kRowBytes
+                                             : ((kk * 32) / 128) * C::kVChunkBytes + ((kk * 32) % 128);
                     const uint64_t d = dv + static_cast<uint64_t>(off >> 4);
-                    if (ESZ == 2) mma_f16_ts(tO, tP + kk * 8, d, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-                    else mma_f8_ts(tO, tP + kk * 8, d, C::kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+                    const uint32_t idesc = RASTER_V ? C::kIdescPVmn : C::kIdescPV;
+                    if (ESZ == 2) mma_f16_ts(tO, tP + kk * 8, d, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+                    else mma_f8_ts(tO, tP + kk * 8, d, idesc, (i > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(bars.o_done));
                 if (i == n_kv - 1) mma_commit(bar(bars.o_final));
@@ -798,7 +818,7 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     }
 }
 
-template <int D, int ESZ, int NS, int TT, int TH, int TW, bool RASTER>
+template <int D, int ESZ, int NS, int TT, int TH, int TW, bool RASTER, bool RASTER_V>
 cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
     using C = Cfg<D, ESZ, NS>;
@@ -807,7 +827,7 @@ cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t st
     static_assert(C::kQHalfWords == 8 || C::kQHalfWords == 16 || C::kQHalfWords == 32, "Q half-row width");
     static_assert(ESZ == 2 || (kColQ + 2 * C::kQHalfWords <= kColP8 && kColP8 + 4 * C::kPHalfWords <= kTmemCols),
                   "TMEM columns of the e4m3 P buffers");
-    auto kern = gna_fwd_kernel<D, ESZ, NS, TT, TH, TW, RASTER>;
+    auto kern = gna_fwd_kernel<D, ESZ, NS, TT, TH, TW, RASTER, RASTER_V>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     kern<<<dim3(static_cast<unsigned>(num_q_tiles)), kThreads, C::kSmemAlloc, stream>>>(p);
@@ -815,14 +835,14 @@ cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t st
 }
 
 // Default tiles get a kernel with the tile shape compiled in.
-template <int D, int ESZ, int NS, bool RASTER>
+template <int D, int ESZ, int NS, bool RASTER, bool RASTER_V = false>
 cudaError_t launch_layout(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
     if (p.tile[0] == 2 && p.tile[1] == 8 && p.tile[2] == 8)
-        return launch_tile<D, ESZ, NS, 2, 8, 8, RASTER>(p, num_q_tiles, stream);
+        return launch_tile<D, ESZ, NS, 2, 8, 8, RASTER, RASTER_V>(p, num_q_tiles, stream);
     if (p.tile[0] == 1 && p.tile[1] == 8 && p.tile[2] == 16)
-        return launch_tile<D, ESZ, NS, 1, 8, 16, RASTER>(p, num_q_tiles, stream);
-    return launch_tile<D, ESZ, NS, 0, 0, 0, RASTER>(p, num_q_tiles, stream);
+        return launch_tile<D, ESZ, NS, 1, 8, 16, RASTER, RASTER_V>(p, num_q_tiles, stream);
+    return launch_tile<D, ESZ, NS, 0, 0, 0, RASTER, RASTER_V>(p, num_q_tiles, stream);
 }
 
 // The raster layout of q, k, out and lse is a separate kernel, so the tiled
@@ -830,6 +850,10 @@ cudaError_t launch_layout(const FwdParams& p, int64_t num_q_tiles, cudaStream_t 
 template <int D, int ESZ, int NS>
 cudaError_t launch_impl(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
+    if constexpr (ESZ == 2 && D == 128) {
+        if (p.raster == 2) return launch_layout<D, ESZ, NS, true, true>(p, num_q_tiles, stream);
+    }
+    if (p.raster == 2) return cudaErrorNotSupported;
     return p.raster ? launch_layout<D, ESZ, NS, true>(p, num_q_tiles, stream)
                     : launch_layout<D, ESZ, NS, false>(p, num_q_tiles, stream);
 }

@@ -37,9 +37,11 @@ cudaError_t launch_permute_v(const void* src, void* dst, const PermuteGeom& g, i
 struct FwdParams {
     CUtensorMap tmK;             // 2-D TMA view [rows, head_dim] of the tiled k, or (raster) the
                                  // 5-D view [B, T, H, W, heads * head_dim] of the raster k
-    CUtensorMap tmV;             // 2-D TMA view [rows * head_dim / 128, 128] of v in the value layout
+    CUtensorMap tmV;             // 2-D TMA view [rows * head_dim / 128, 128] of v in the value layout, or
+                                 // (raster == 2) the 5-D view of the raster v, like tmK
     const void* q;               // tiled q [rows, head_dim], or raster q (read row by row into TMEM)
-    int raster;                  // 1: q, k, out and lse use the raster layout (v stays in the value layout)
+    int raster;                  // 1: q, k, out and lse use the raster layout (v in the value layout);
+                                 // 2: v too (bf16, head_dim 128)
     void* out;                   // tiled bf16 [rows, head_dim]
     float* lse;                  // tiled float [rows] or nullptr
     const float* descale;        // e4m3 only: 3 device floats (q, k, v) or nullptr

@@ -93,6 +93,8 @@ def lib() -> ctypes.CDLL:
                                      ctypes.POINTER(GNAOptions), _P]
         L.gna_forward_raster.restype = st
         L.gna_forward_raster.argtypes = L.gna_forward_ex.argtypes
+        L.gna_forward_raster_all.restype = st
+        L.gna_forward_raster_all.argtypes = L.gna_forward_ex.argtypes
         L.gna_forward_fp8.restype = st
         L.gna_forward_fp8.argtypes = [_P, _P, _P, _P, _P, _INT, _INT, _I3, _I3, _I3, _INT, _P, _P]
         L.gna_permuted_elems.restype = ctypes.c_size_t
@@ -376,6 +378,31 @@ def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, 
     _check(lib().gna_forward_raster(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                     _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
                                     _stream_ptr(stream, dev)))
+
+
+def gna_forward_raster_all(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                           lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int, *,
+                           tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, stream=None):
+    """GNA forward with every tensor in the raster layout (see ``include/gna.h``):
+    q, k, v bf16 ``[B, T, H, W, heads, 128]``, ``out`` bf16 raster, ``lse`` float32
+    ``[B, T, H, W, heads]`` or None.  No permute; slower P V than
+    :func:`gna_forward_raster` with v in the value layout."""
+    code = dtype_code(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise ValueError("q, k, v must share a dtype")
+    if out.dtype != torch.bfloat16:
+        raise ValueError("out must be bfloat16")
+    if lse is not None and lse.dtype != torch.float32:
+        raise ValueError("lse must be float32")
+    nr = _raster_elems(B, heads, dims, head_dim)
+    dev = _need(q=(q, nr), k=(k, nr), v=(v, nr), out=(out, nr), lse=(lse, nr // head_dim))
+    opt = GNAOptions()
+    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+    opt.leader_rule = leader_rule
+    opt.scale = scale
+    _check(lib().gna_forward_raster_all(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
+                                        _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
+                                        _stream_ptr(stream, dev)))
 
 
 def gna_backward_delta(out: torch.Tensor, dout: torch.Tensor, delta: torch.Tensor, B: int, heads: int, dims,

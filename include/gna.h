@@ -216,6 +216,19 @@ gna_status gna_forward_raster(const void* q, const void* k, const void* v_value,
                               int B, int heads, const int dims[3], const int window[3], const int stride[3],
                               int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
 
+/* gna_forward_raster with V in the raster layout as well: no permute at all
+ * (GNA page §2.2: the permutation before and after the model is memory work
+ * the page plans to remove).  v is raster [B, T, H, W, heads, head_dim]; the
+ * kernel loads each V tile like K (a 5-D TMA box) and P V reads it token-major,
+ * an operand order the tensor core streams more slowly than the value layout
+ * of gna_forward_raster (about 930 against 600 cycles per 128-token tile on one
+ * SM), so this call trades forward speed for the V permute it saves.
+ * GNA_BF16 with head_dim 128 only (otherwise GNA_ERR_UNSUPPORTED); everything
+ * else as gna_forward_raster. */
+gna_status gna_forward_raster_all(const void* q, const void* k, const void* v, void* out, float* lse,
+                                  int B, int heads, const int dims[3], const int window[3], const int stride[3],
+                                  int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
+
 /* ------------------------------------------------------------ backward ---- */
 
 /* The GNA page asks for GNA in training (§4.2, problem 1; §5) and writes no

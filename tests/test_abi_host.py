@@ -132,6 +132,16 @@ def test_failure_injection_is_an_explicit_call(L):
     assert "getenv" not in src
 
 
+def test_forward_raster_all_supports_bf16_head_dim_128_only(L):
+    geom = (1, 2, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1))
+    assert L.gna_forward_raster_all(FAKE, FAKE, FAKE, FAKE, None, *geom, 64, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_UNSUPPORTED
+    assert L.gna_forward_raster_all(FAKE, FAKE, FAKE, FAKE, None, *geom, 128, G.GNA_FP8_E4M3, None, None) == \
+        G.GNA_ERR_UNSUPPORTED
+    assert L.gna_forward_raster_all(FAKE, FAKE, FAKE + 8, FAKE, None, *geom, 128, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_INVALID_ARG
+
+
 def test_forward_raster_rejects_bad_arguments_on_host(L):
     args = (1, 2, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1), 32, G.GNA_BF16, None, None)
     assert L.gna_forward_raster(None, FAKE, FAKE, FAKE, None, *args) == G.GNA_ERR_INVALID_ARG
