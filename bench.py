@@ -61,6 +61,9 @@ def parse_args(argv=None):
                     help="tiled: permute Q, K, V and unpermute O, lse around gna_forward; "
                          "raster: permute V only, gna_forward_raster on raster Q, K, O, lse; "
                          "raster_all: no permute, gna_forward_raster_all on raster Q, K, V, O, lse (bf16, d 128)")
+    ap.add_argument("--tiles", default="default", choices=["default", "planned"],
+                    help="default: one tile for Q and KV (gna_tile_shape); planned: the query and key/value "
+                         "tiles gna_plan_tiles picks (they may differ; forward only)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true")
     ap.add_argument("--sustain", type=float, default=0.0,
@@ -97,7 +100,7 @@ def run_config(a, world: int = 1) -> dict:
     esz = 2 if a.dtype == "bf16" else 1
     return {"workload": workload_name(a), "dims": list(a.dims), "window": list(a.window),
             "stride": list(a.stride), "heads": a.heads, "B": a.batch, "head_dim": a.head_dim,
-            "layout": a.layout,
+            "layout": a.layout, "tiles": a.tiles,
             "l2": "inputs larger than L2 (3 x %.0f MB raster + tiled copies)" % (
                 a.batch * math.prod(a.dims) * a.heads * a.head_dim * esz / 1e6),
             "parallelism": f"replicas x{world}: every rank runs the full workload on its own data"}
@@ -178,7 +181,7 @@ def kernel_traffic(a) -> int | None:
     m = rec.get("match", {})
     same = (list(a.dims) == m.get("dims") and list(a.window) == m.get("window") and list(a.stride) == m.get("stride")
             and a.head_dim == m.get("head_dim") and a.dtype == m.get("dtype"))
-    if rec.get("source_sha256") != h or not same or a.layout not in rec.get("layouts", {}):
+    if rec.get("source_sha256") != h or not same or a.layout not in rec.get("layouts", {}) or a.tiles != "default":
         return None
     return rec["layouts"][a.layout]["bytes_per_plane"] * a.heads * a.batch
 
@@ -385,13 +388,19 @@ def gpu_arm(a, rank, world, local):
     ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)
     raster = a.layout in ("raster", "raster_all")
     raster_v = a.layout == "raster_all"
-    shp = G.tiled_shape(B, heads, dims, d)
+    # query tile and key/value tile (None: the default tile for both)
+    tq = tkv = None
+    if a.tiles == "planned":
+        tq, tkv, _, _ = G.gna_plan_tiles(dims, a.window, a.stride)
+    shp = G.tiled_shape(B, heads, dims, d, tq)
+    shp_kv = G.tiled_shape(B, heads, dims, d, tkv)
     if not raster:                      # the raster path has no tiled Q, K, O or lse
-        qt, kt = (torch.empty(shp, dtype=dt, device=dev) for _ in range(2))
+        qt = torch.empty(shp, dtype=dt, device=dev)
+        kt = torch.empty(shp_kv, dtype=dt, device=dev)
         out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
         lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     if not raster_v:                    # the all-raster path reads V as it is
-        vt = torch.empty(G.value_shape(B, heads, dims, d), dtype=dt, device=dev)
+        vt = torch.empty(G.value_shape(B, heads, dims, d, tkv), dtype=dt, device=dev)
     out = torch.empty(raster_shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(raster_shape[:-1] + (1,), dtype=torch.float32, device=dev)
 
@@ -399,24 +408,25 @@ def gpu_arm(a, rank, world, local):
         """One forward launch of the bench's layout (raster tensors in, raster out)."""
         if raster_v:
             G.gna_forward_raster_all(q_in, k_in, xs[2] if v_in is None else v_in, o_dst, lse_dst[..., 0], B, heads,
-                                     dims, window, stride, d, stream=stream)
+                                     dims, window, stride, d, tile=tq, tile_kv=tkv, stream=stream)
         elif raster:
             G.gna_forward_raster(q_in, k_in, vt, o_dst, lse_dst[..., 0], B, heads, dims, window, stride, d,
-                                 descale=ds, stream=stream)
+                                 descale=ds, tile=tq, tile_kv=tkv, stream=stream)
         else:
-            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, window, stride, d, descale=ds, stream=stream)
+            G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, window, stride, d, descale=ds, tile=tq,
+                          tile_kv=tkv, stream=stream)
 
     def permute_in(q_in, k_in, v_in):
         if not raster:
-            G.gna_permute(q_in, qt, B, heads, dims, d, stream=stream)
-            G.gna_permute(k_in, kt, B, heads, dims, d, stream=stream)
+            G.gna_permute(q_in, qt, B, heads, dims, d, tile=tq, stream=stream)
+            G.gna_permute(k_in, kt, B, heads, dims, d, tile=tkv, stream=stream)
         if not raster_v:
-            G.gna_permute_v(v_in, vt, B, heads, dims, d, stream=stream)
+            G.gna_permute_v(v_in, vt, B, heads, dims, d, tile=tkv, stream=stream)
 
     def unpermute_out(o_dst, lse_dst):
         if not raster:
-            G.gna_unpermute(out_t, o_dst, B, heads, dims, d, stream=stream)
-            G.gna_unpermute(lse_t.unsqueeze(-1), lse_dst, B, heads, dims, 1, stream=stream)
+            G.gna_unpermute(out_t, o_dst, B, heads, dims, d, tile=tq, stream=stream)
+            G.gna_unpermute(lse_t.unsqueeze(-1), lse_dst, B, heads, dims, 1, tile=tq, stream=stream)
 
     ev = {"fwd": [], "perm": [], "unperm": []}
 
@@ -489,7 +499,7 @@ def gpu_arm(a, rank, world, local):
         peak_source = "measured e4m3 cuBLASLt GEMM burst (profiles/e4m3_gemm_peak.json)"
 
     # tile-level work of the launch (what the tensor cores execute)
-    visited, partial, nq = G.gna_tile_stats(dims, a.window, a.stride)
+    visited, partial, nq = G.gna_tile_stats(dims, a.window, a.stride, tq, tile_kv=tkv)
     tile_flops = 4.0 * B * heads * visited * 128 * 128 * d
 
     # dense attention through the same kernel on the same tokens (window = grid)
@@ -609,7 +619,7 @@ def gpu_arm(a, rank, world, local):
     # optional: the backward pass on the same workload, inputs resident (tiled
     # q, k, v, dout; k in the value layout; the forward's out and lse)
     backward = None
-    if a.backward and a.dtype == "bf16" and d == 128 and not raster:
+    if a.backward and a.dtype == "bf16" and d == 128 and not raster and a.tiles == "default":
         v_tiled = torch.empty(shp, dtype=dt, device=dev)
         k_val = torch.empty_like(vt)
         G.gna_permute(xs[2], v_tiled, B, heads, dims, d, stream=stream)
@@ -668,7 +678,8 @@ def gpu_arm(a, rank, world, local):
         "warmup": a.warmup, "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": a.dtype,
         "data": "synthetic: iid N(0,1) Q/K/V drawn on the device per rank",
-        "config": run_config(a, world), "tile": list(G.gna_tile_shape(dims)),
+        "config": run_config(a, world), "tile": list(tq or G.gna_tile_shape(dims)),
+        "tile_kv": list(tkv or tq or G.gna_tile_shape(dims)),
         "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak_burst, "unit": "TFLOP/s",
                      "frac": kernel_tflops / peak_burst, "traffic": traffic,
                      "peak_source": peak_source,
@@ -683,7 +694,8 @@ def gpu_arm(a, rank, world, local):
         "dense_forward_ms": dense_ms, "speedup_vs_dense": speedup,
         "dense_clocks": dense_clk, "speedup_vs_dense_clock_normalised": speedup_clock_normalised,
         "flop_sparsity_ratio": n_ratio,
-        "speedup_bound_at_equal_tile_rate": G.gna_plan_tile(dims, a.window, a.stride)[2],
+        "speedup_bound_at_equal_tile_rate": (G.gna_plan_tiles(dims, a.window, a.stride)[3] if a.tiles == "planned"
+                                             else G.gna_plan_tile(dims, a.window, a.stride)[2]),
         "speedup_over_ratio": None if speedup is None else speedup / n_ratio,
         "e2e": e2e, "gpu_launches": launches_per_step * a.steps, "clocks": clk, "cpu_baseline": cpu,
         "sustained": sustained, "backward": backward,

@@ -375,29 +375,30 @@ gna_status gna_unpermute_v_tiled(const void* src, void* dst, int B, int heads, c
     return permute_common(src, dst, B, heads, dims, tile, head_dim, dtype, stream, false, true);
 }
 
-gna_status gna_tile_stats(const int dims[3], const int window[3], const int stride[3], const int tile_in[3],
-                          int leader_rule, int64_t* visited_kv_tiles, int64_t* partial_kv_tiles, int64_t* q_tiles)
+gna_status gna_tile_stats_qkv(const int dims[3], const int window[3], const int stride[3], const int tile_q_in[3],
+                              const int tile_kv_in[3], int leader_rule, int64_t* visited_kv_tiles,
+                              int64_t* partial_kv_tiles, int64_t* q_tiles)
 {
     gna_status st = check_geometry(dims, window, stride);
     if (st != GNA_OK) return st;
     if (leader_rule != GNA_LEADER_CENTER && leader_rule != GNA_LEADER_LITERAL)
         return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", leader_rule);
-    int tile[3], tlog[3];
-    st = resolve_tile(dims, tile_in, tile, tlog);
-    if (st != GNA_OK) return st;
+    int tq[3], tkv[3], tlog[3];
+    if ((st = resolve_tile(dims, tile_q_in, tq, tlog)) != GNA_OK) return st;
+    if ((st = resolve_tile(dims, tile_kv_in, tkv, tlog)) != GNA_OK) return st;
     // The visited box of a Q tile is a product of per-dimension ranges, so
     // the totals over all Q tiles factor into per-dimension sums.
     int64_t visited = 1, full = 1, nq = 1;
     for (int d = 0; d < 3; ++d) {
-        const int nt = (dims[d] + tile[d] - 1) / tile[d];
+        const int nt = (dims[d] + tq[d] - 1) / tq[d];
         const int off = gna::leader_offset(stride[d], leader_rule);
         int64_t sum_cnt = 0, sum_full = 0;
         for (int qt = 0; qt < nt; ++qt) {
-            const gna::DimRange r = gna::dim_range(qt, tile[d], dims[d], window[d], stride[d], off);
+            const gna::DimRange r = gna::dim_range(qt, tq[d], tkv[d], dims[d], window[d], stride[d], off);
             sum_cnt += r.k1 - r.k0 + 1;
             // the kernel's full-tile test: the interval form of dim_tile_full
             int flo, fhi;
-            gna::dim_full_range(tile[d], dims[d], window[d], r, flo, fhi);
+            gna::dim_full_range(tkv[d], dims[d], window[d], r, flo, fhi);
             for (int kt = r.k0; kt <= r.k1; ++kt) sum_full += (kt >= flo && kt <= fhi);
         }
         visited *= sum_cnt;
@@ -408,6 +409,13 @@ gna_status gna_tile_stats(const int dims[3], const int window[3], const int stri
     if (partial_kv_tiles) *partial_kv_tiles = visited - full;
     if (q_tiles) *q_tiles = nq;
     return GNA_OK;
+}
+
+gna_status gna_tile_stats(const int dims[3], const int window[3], const int stride[3], const int tile_in[3],
+                          int leader_rule, int64_t* visited_kv_tiles, int64_t* partial_kv_tiles, int64_t* q_tiles)
+{
+    return gna_tile_stats_qkv(dims, window, stride, tile_in, tile_in, leader_rule, visited_kv_tiles,
+                              partial_kv_tiles, q_tiles);
 }
 
 gna_status gna_plan_tile(const int dims[3], const int window[3], const int stride[3], int leader_rule, int tile[3],
@@ -454,6 +462,54 @@ gna_status gna_plan_tile(const int dims[3], const int window[3], const int strid
     return GNA_OK;
 }
 
+gna_status gna_plan_tiles(const int dims[3], const int window[3], const int stride[3], int leader_rule,
+                          int tile_q[3], int tile_kv[3], double* tile_overhead, double* speedup_bound)
+{
+    gna_status st = check_geometry(dims, window, stride);
+    if (st != GNA_OK) return st;
+    if (tile_q == nullptr || tile_kv == nullptr) return fail(GNA_ERR_INVALID_ARG, "tile is NULL");
+    if (leader_rule != GNA_LEADER_CENTER && leader_rule != GNA_LEADER_LITERAL)
+        return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", leader_rule);
+    // start from the best equal pair, so that a decoupled pair is chosen only
+    // when it visits strictly fewer tile pairs, or as many with fewer partial ones
+    int eq[3];
+    if ((st = gna_plan_tile(dims, window, stride, leader_rule, eq, nullptr, nullptr)) != GNA_OK) return st;
+    int64_t best_v = 0, best_p = 0;
+    if ((st = gna_tile_stats(dims, window, stride, eq, leader_rule, &best_v, &best_p, nullptr)) != GNA_OK) return st;
+    int bq[3] = {eq[0], eq[1], eq[2]}, bk[3] = {eq[0], eq[1], eq[2]};
+    for (int qt = 0; qt <= 7; ++qt)
+        for (int qh = 0; qt + qh <= 7; ++qh)
+            for (int kt = 0; kt <= 7; ++kt)
+                for (int kh = 0; kt + kh <= 7; ++kh) {
+                    const int tq[3] = {1 << qt, 1 << qh, 1 << (7 - qt - qh)};
+                    const int tk[3] = {1 << kt, 1 << kh, 1 << (7 - kt - kh)};
+                    int64_t v = 0, pa = 0;
+                    if (gna_tile_stats_qkv(dims, window, stride, tq, tk, leader_rule, &v, &pa, nullptr) != GNA_OK)
+                        continue;
+                    if (v < best_v || (v == best_v && pa < best_p)) {
+                        best_v = v;
+                        best_p = pa;
+                        for (int d = 0; d < 3; ++d) {
+                            bq[d] = tq[d];
+                            bk[d] = tk[d];
+                        }
+                    }
+                }
+    double useful = 1.0, tiles_q = 1.0, tiles_kv = 1.0;
+    for (int d = 0; d < 3; ++d) {
+        tile_q[d] = bq[d];
+        tile_kv[d] = bk[d];
+        useful *= static_cast<double>(dims[d]) * window[d];
+        tiles_q *= (dims[d] + bq[d] - 1) / bq[d];
+        tiles_kv *= (dims[d] + bk[d] - 1) / bk[d];
+    }
+    const double tile_pairs = static_cast<double>(gna::kTileElems) * gna::kTileElems;
+    if (tile_overhead) *tile_overhead = static_cast<double>(best_v) * tile_pairs / useful;
+    if (speedup_bound) *speedup_bound = tiles_q * tiles_kv / static_cast<double>(best_v);
+    t_last_error.clear();
+    return GNA_OK;
+}
+
 namespace {
 
 // raster: 0 = tiled q, k, out, lse; 1 = raster q, k, out, lse; 2 = raster v as well
@@ -488,10 +544,14 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
         return fail(GNA_ERR_INVALID_ARG, "descale must be 4-byte aligned");
 
     gna::FwdParams p{};
-    int tlog[3];
-    st = resolve_tile(dims, opt ? opt->tile : nullptr, p.tile, tlog);
+    int tlog[3], tlog_q[3];
+    st = resolve_tile(dims, opt ? opt->tile : nullptr, p.tile_q, tlog_q);
     if (st != GNA_OK) return st;
-    int64_t tiles_per_head = 1;
+    // key / value tile: opt->tile_kv when set, else the query tile
+    const bool kv_own = opt && (opt->tile_kv[0] != 0 || opt->tile_kv[1] != 0 || opt->tile_kv[2] != 0);
+    st = resolve_tile(dims, kv_own ? opt->tile_kv : p.tile_q, p.tile, tlog);
+    if (st != GNA_OK) return st;
+    int64_t tiles_per_head = 1, tiles_per_head_q = 1;
     for (int d = 0; d < 3; ++d) {
         p.dims[d] = dims[d];
         p.win[d] = window[d];
@@ -500,12 +560,18 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
         p.tlog[d] = tlog[d];
         p.nt[d] = (dims[d] + p.tile[d] - 1) / p.tile[d];
         tiles_per_head *= p.nt[d];
+        p.tlog_q[d] = tlog_q[d];
+        p.nt_q[d] = (dims[d] + p.tile_q[d] - 1) / p.tile_q[d];
+        tiles_per_head_q *= p.nt_q[d];
     }
-    const int64_t num_q_tiles = tiles_per_head * B * heads;
+    const int64_t num_q_tiles = tiles_per_head_q * B * heads;
+    const int64_t num_kv_tiles = tiles_per_head * B * heads;
     const int64_t rows = num_q_tiles * gna::kTileElems;
-    if (rows > INT32_MAX) return fail(GNA_ERR_UNSUPPORTED, "more than 2^31 tiled rows");
+    const int64_t rows_kv = num_kv_tiles * gna::kTileElems;
+    if (rows > INT32_MAX || rows_kv > INT32_MAX) return fail(GNA_ERR_UNSUPPORTED, "more than 2^31 tiled rows");
     p.heads = heads;
     p.tiles_per_head = static_cast<int>(tiles_per_head);
+    p.tiles_per_head_q = static_cast<int>(tiles_per_head_q);
     p.out = out;
     p.lse = lse;
     p.descale = (opt && es == 1) ? opt->descale : nullptr;
@@ -518,12 +584,12 @@ gna_status forward_impl(const void* q, const void* k, const void* v, void* out, 
         if (static_cast<int64_t>(B) * dims[0] > INT32_MAX || static_cast<int64_t>(heads) * head_dim > INT32_MAX)
             return fail(GNA_ERR_UNSUPPORTED, "raster tensor too large for TMA coordinates");
         if ((st = make_raster_map(&p.tmK, k, B, dims, heads, head_dim, es, p.tile)) != GNA_OK) return st;
-    } else if ((st = make_tile_map(&p.tmK, k, rows, head_dim, es)) != GNA_OK) {
+    } else if ((st = make_tile_map(&p.tmK, k, rows_kv, head_dim, es)) != GNA_OK) {
         return st;
     }
     if (raster == 2) {
         if ((st = make_raster_map(&p.tmV, v, B, dims, heads, head_dim, es, p.tile)) != GNA_OK) return st;
-    } else if ((st = make_value_map(&p.tmV, v, num_q_tiles, head_dim, es)) != GNA_OK) {
+    } else if ((st = make_value_map(&p.tmV, v, num_kv_tiles, head_dim, es)) != GNA_OK) {
         return st;
     }
 
@@ -639,6 +705,9 @@ gna_status backward_common(int B, int heads, const int dims[3], const int window
     if (opt && opt->descale) return fail(GNA_ERR_INVALID_ARG, "descale is only used with GNA_FP8_E4M3");
     st = resolve_tile(dims, opt ? opt->tile : nullptr, tile, tlog);
     if (st != GNA_OK) return st;
+    if (opt && (opt->tile_kv[0] != 0 || opt->tile_kv[1] != 0 || opt->tile_kv[2] != 0) &&
+        (opt->tile_kv[0] != tile[0] || opt->tile_kv[1] != tile[1] || opt->tile_kv[2] != tile[2]))
+        return fail(GNA_ERR_UNSUPPORTED, "the backward pass needs the key/value tile equal to the query tile");
     int64_t n = static_cast<int64_t>(B) * heads;
     for (int d = 0; d < 3; ++d) n *= (dims[d] + tile[d] - 1) / tile[d];
     if (n * gna::kTileElems > INT32_MAX) return fail(GNA_ERR_UNSUPPORTED, "more than 2^31 tiled rows");

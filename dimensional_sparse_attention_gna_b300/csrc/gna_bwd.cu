@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
     BwdBox box;
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
-        const DimRange r = dim_range(qc[d], p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
+        const DimRange r = dim_range(qc[d], p.tile[d], p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
         box.k0[d] = r.k0;
         box.cnt[d] = r.k1 - r.k0 + 1;
         dim_full_range(p.tile[d], p.dims[d], p.win[d], r, box.full_lo[d], box.full_hi[d]);
@@ -558,7 +558,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
     for (int d = 0; d < 3; ++d) {
         int lo = -1, hi = -2;
         for (int qt = 0; qt < p.nt[d]; ++qt) {
-            const DimRange r = dim_range(qt, p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
+            const DimRange r = dim_range(qt, p.tile[d], p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
             if (r.k0 <= kc[d] && kc[d] <= r.k1) {
                 if (lo < 0) lo = qt;
                 hi = qt;

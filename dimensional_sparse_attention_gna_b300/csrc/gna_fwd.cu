@@ -344,17 +344,17 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
     const int lane = threadIdx.x % 32;
 
     // ---------------------------------------------------------------- tile geometry (all threads)
-    const int64_t q_tile_global = blockIdx.x;                 // (b*heads + h)*tiles_per_head + qt
-    const int qt_id = static_cast<int>(q_tile_global % p.tiles_per_head);
-    const int64_t bh = q_tile_global / p.tiles_per_head;
+    const int64_t q_tile_global = blockIdx.x;                 // (b*heads + h)*tiles_per_head_q + qt
+    const int qt_id = static_cast<int>(q_tile_global % p.tiles_per_head_q);
+    const int64_t bh = q_tile_global / p.tiles_per_head_q;
     int qc[3];
-    qc[2] = qt_id % p.nt[2];
-    qc[1] = (qt_id / p.nt[2]) % p.nt[1];
-    qc[0] = qt_id / (p.nt[2] * p.nt[1]);
+    qc[2] = qt_id % p.nt_q[2];
+    qc[1] = (qt_id / p.nt_q[2]) % p.nt_q[1];
+    qc[0] = qt_id / (p.nt_q[2] * p.nt_q[1]);
     KvBox box;
 #pragma unroll
     for (int d = 0; d < 3; ++d) {
-        const DimRange r = dim_range(qc[d], p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
+        const DimRange r = dim_range(qc[d], p.tile_q[d], p.tile[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
         box.k0[d] = r.k0;
         box.cnt[d] = r.k1 - r.k0 + 1;
         dim_full_range(p.tile[d], p.dims[d], p.win[d], r, box.full_lo[d], box.full_hi[d]);
@@ -553,12 +553,12 @@ __global__ void __launch_bounds__(kThreads, 1) gna_fwd_kernel(const __grid_const
         // query coordinates of this row
         int qpos[3], st[3];
         {
-            const int ix = row & (p.tile[2] - 1);
-            const int iy = (row >> p.tlog[2]) & (p.tile[1] - 1);
-            const int it = row >> (p.tlog[1] + p.tlog[2]);
-            qpos[0] = qc[0] * p.tile[0] + it;
-            qpos[1] = qc[1] * p.tile[1] + iy;
-            qpos[2] = qc[2] * p.tile[2] + ix;
+            const int ix = row & (p.tile_q[2] - 1);
+            const int iy = (row >> p.tlog_q[2]) & (p.tile_q[1] - 1);
+            const int it = row >> (p.tlog_q[1] + p.tlog_q[2]);
+            qpos[0] = qc[0] * p.tile_q[0] + it;
+            qpos[1] = qc[1] * p.tile_q[1] + iy;
+            qpos[2] = qc[2] * p.tile_q[2] + ix;
         }
         const bool row_valid = qpos[0] < p.dims[0] && qpos[1] < p.dims[1] && qpos[2] < p.dims[2];
         // row of this query in the tensor q / out / lse are stored in
@@ -834,7 +834,9 @@ cudaError_t launch_tile(const FwdParams& p, int64_t num_q_tiles, cudaStream_t st
     return cudaGetLastError();
 }
 
-// Default tiles get a kernel with the tile shape compiled in.
+// The default tiles, and (head_dim 128) the key/value tiles the pair planner
+// picks for the video latent, get a kernel with the KV tile shape compiled into
+// the mask code; any other tile runs the generic mask.
 template <int D, int ESZ, int NS, bool RASTER, bool RASTER_V = false>
 cudaError_t launch_layout(const FwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
@@ -842,6 +844,12 @@ cudaError_t launch_layout(const FwdParams& p, int64_t num_q_tiles, cudaStream_t 
         return launch_tile<D, ESZ, NS, 2, 8, 8, RASTER, RASTER_V>(p, num_q_tiles, stream);
     if (p.tile[0] == 1 && p.tile[1] == 8 && p.tile[2] == 16)
         return launch_tile<D, ESZ, NS, 1, 8, 16, RASTER, RASTER_V>(p, num_q_tiles, stream);
+    if constexpr (D == 128) {
+        if (p.tile[0] == 2 && p.tile[1] == 4 && p.tile[2] == 16)
+            return launch_tile<D, ESZ, NS, 2, 4, 16, RASTER, RASTER_V>(p, num_q_tiles, stream);
+        if (p.tile[0] == 4 && p.tile[1] == 4 && p.tile[2] == 8)
+            return launch_tile<D, ESZ, NS, 4, 4, 8, RASTER, RASTER_V>(p, num_q_tiles, stream);
+    }
     return launch_tile<D, ESZ, NS, 0, 0, 0, RASTER, RASTER_V>(p, num_q_tiles, stream);
 }
 

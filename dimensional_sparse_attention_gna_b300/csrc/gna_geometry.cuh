@@ -38,22 +38,23 @@ __host__ __device__ __forceinline__ int leader_offset(int s, int rule)
 }
 
 // Range of KV tiles (inclusive) and the window-start extremes of the query
-// tile `qt` along one dimension.
+// tile `qt` along one dimension.  Query tiles have extent tq, KV tiles extent
+// tkv (equal unless the two tilings are chosen separately, GNA page §1.2).
 struct DimRange {
     int k0, k1;        // first / last KV tile index visited
     int smin, smax;    // window start of the first / last valid query
 };
 
-__host__ __device__ __forceinline__ DimRange dim_range(int qt, int t, int L, int w, int s, int off)
+__host__ __device__ __forceinline__ DimRange dim_range(int qt, int tq, int tkv, int L, int w, int s, int off)
 {
-    int lo = qt * t;
-    int hi = lo + t - 1;
+    int lo = qt * tq;
+    int hi = lo + tq - 1;
     hi = hi < L - 1 ? hi : L - 1;
     DimRange r;
     r.smin = window_start(lo, L, w, s, off);
     r.smax = window_start(hi, L, w, s, off);
-    r.k0 = r.smin / t;
-    r.k1 = (r.smax + w - 1) / t;
+    r.k0 = r.smin / tkv;
+    r.k1 = (r.smax + w - 1) / tkv;
     return r;
 }
 

@@ -46,9 +46,11 @@ struct FwdParams {
     float* lse;                  // tiled float [rows] or nullptr
     const float* descale;        // e4m3 only: 3 device floats (q, k, v) or nullptr
     int dims[3], win[3], str[3], off[3];
-    int tile[3], tlog[3], nt[3];
+    int tile[3], tlog[3], nt[3];  // key / value tiles (layout of k and v, the KV tile box)
+    int tile_q[3], tlog_q[3], nt_q[3];   // query tiles (layout of q, out and lse; one per CTA)
     int heads;
-    int tiles_per_head;          // nt[0] * nt[1] * nt[2]
+    int tiles_per_head;          // KV tiles per (b, head) plane: nt[0] * nt[1] * nt[2]
+    int tiles_per_head_q;        // query tiles per plane: nt_q[0] * nt_q[1] * nt_q[2]
     float scale;                 // softmax scale
     int fault_skip_kv;           // test hook: >= 0 makes the producer skip that KV load
 };

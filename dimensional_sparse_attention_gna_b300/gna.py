@@ -50,7 +50,7 @@ def _status_name(s: int) -> str:
 
 class GNAOptions(ctypes.Structure):
     _fields_ = [("tile", ctypes.c_int * 3), ("leader_rule", ctypes.c_int), ("scale", ctypes.c_float),
-                ("descale", ctypes.c_void_p)]
+                ("descale", ctypes.c_void_p), ("tile_kv", ctypes.c_int * 3)]
 
 
 _lib = None
@@ -118,6 +118,12 @@ def lib() -> ctypes.CDLL:
         L.gna_plan_tile.restype = st
         L.gna_plan_tile.argtypes = [_I3, _I3, _I3, _INT, _I3, ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_double)]
+        L.gna_tile_stats_qkv.restype = st
+        L.gna_tile_stats_qkv.argtypes = [_I3, _I3, _I3, _P, _P, _INT, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                         ctypes.POINTER(i64)]
+        L.gna_plan_tiles.restype = st
+        L.gna_plan_tiles.argtypes = [_I3, _I3, _I3, _INT, _I3, _I3, ctypes.POINTER(ctypes.c_double),
+                                     ctypes.POINTER(ctypes.c_double)]
         L.gna_schedule_step.restype = st
         L.gna_schedule_step.argtypes = [_INT, _INT, _INT, _I3, _I3, _I3, _I3, _I3]
         L.gna_get_status.restype = st
@@ -286,6 +292,16 @@ def gna_unpermute_v(src: torch.Tensor, dst: torch.Tensor, B: int, heads: int, di
     _check(st)
 
 
+def _options(tile, leader_rule: int, scale: float, descale: torch.Tensor | None, tile_kv=None) -> GNAOptions:
+    opt = GNAOptions()
+    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
+    opt.leader_rule = leader_rule
+    opt.scale = scale
+    opt.descale = _ptr(descale)
+    opt.tile_kv = (ctypes.c_int * 3)(*(tile_kv or (0, 0, 0)))
+    return opt
+
+
 def _descale_arg(descale: torch.Tensor | None) -> torch.Tensor | None:
     if descale is not None and (descale.dtype != torch.float32 or descale.numel() != 3):
         raise ValueError("descale must be 3 float32 values")
@@ -295,16 +311,17 @@ def _descale_arg(descale: torch.Tensor | None) -> torch.Tensor | None:
 def gna_forward(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out: torch.Tensor,
                 lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int, *, tile=None,
                 leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, descale: torch.Tensor | None = None,
-                stream=None):
+                tile_kv=None, stream=None):
     """GNA forward on tiled tensors (see ``include/gna.h``).
 
     ``q, k``: bf16 or float8_e4m3fn, tiled; ``v_value``: same dtype, V in the
     VALUE layout (:func:`gna_permute_v`, not :func:`gna_permute`); ``out``:
     bf16 tiled; ``lse``: float32 ``[B, heads, tiles, 128]`` or None;
     ``descale``: float32 device tensor of 3 values, required for e4m3 and
-    refused for bf16.  The plain bf16 call goes to ``gna_forward``, an e4m3
-    call with default options to ``gna_forward_fp8``, anything else to
-    ``gna_forward_ex``.
+    refused for bf16; ``tile_kv``: the tile of ``k`` and ``v_value`` when it
+    differs from ``tile`` (the tile of ``q``, ``out``, ``lse``).  The plain bf16
+    call goes to ``gna_forward``, an e4m3 call with default options to
+    ``gna_forward_fp8``, anything else to ``gna_forward_ex``.
     """
     code = dtype_code(q.dtype)
     if k.dtype != q.dtype or v_value.dtype != q.dtype:
@@ -315,10 +332,11 @@ def gna_forward(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out: to
         raise ValueError("lse must be float32")
     descale = _descale_arg(descale)
     nt = gna_tiled_elems(B, heads, dims, head_dim, tile)
-    dev = _need(q=(q, nt), k=(k, nt), v_value=(v_value, nt), out=(out, nt), lse=(lse, nt // head_dim),
+    nkv = gna_tiled_elems(B, heads, dims, head_dim, tile_kv if tile_kv is not None else tile)
+    dev = _need(q=(q, nt), k=(k, nkv), v_value=(v_value, nkv), out=(out, nt), lse=(lse, nt // head_dim),
                 descale=(descale, 3))
     st_ptr = _stream_ptr(stream, dev)
-    defaults = tile is None and leader_rule == GNA_LEADER_CENTER and scale == 0.0
+    defaults = tile is None and tile_kv is None and leader_rule == GNA_LEADER_CENTER and scale == 0.0
     if defaults and code == GNA_BF16 and descale is None:
         st = lib().gna_forward(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                _I3(*window), _I3(*stride), head_dim, code, st_ptr)
@@ -326,11 +344,7 @@ def gna_forward(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out: to
         st = lib().gna_forward_fp8(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                    _I3(*window), _I3(*stride), head_dim, _ptr(descale), st_ptr)
     else:
-        opt = GNAOptions()
-        opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
-        opt.leader_rule = leader_rule
-        opt.scale = scale
-        opt.descale = _ptr(descale)
+        opt = _options(tile, leader_rule, scale, descale, tile_kv)
         st = lib().gna_forward_ex(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                   _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt), st_ptr)
     _check(st)
@@ -351,13 +365,13 @@ def gna_forward_fp8(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out
 def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, out: torch.Tensor,
                        lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int, *,
                        tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0,
-                       descale: torch.Tensor | None = None, stream=None):
+                       descale: torch.Tensor | None = None, tile_kv=None, stream=None):
     """GNA forward with q, k, out and lse in the raster layout (see ``include/gna.h``).
 
     ``q, k``: bf16 or float8_e4m3fn ``[B, T, H, W, heads, head_dim]``;
-    ``v_value``: same dtype, value layout (:func:`gna_permute_v` with the same
-    ``tile``); ``out``: bf16 raster; ``lse``: float32 ``[B, T, H, W, heads]``
-    or None; ``descale`` as for :func:`gna_forward`.
+    ``v_value``: same dtype, value layout (:func:`gna_permute_v` with
+    ``tile_kv``, else ``tile``); ``out``: bf16 raster; ``lse``: float32
+    ``[B, T, H, W, heads]`` or None; ``descale`` as for :func:`gna_forward`.
     """
     code = dtype_code(q.dtype)
     if k.dtype != q.dtype or v_value.dtype != q.dtype:
@@ -368,13 +382,10 @@ def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, 
         raise ValueError("lse must be float32")
     descale = _descale_arg(descale)
     nr = _raster_elems(B, heads, dims, head_dim)
-    dev = _need(q=(q, nr), k=(k, nr), v_value=(v_value, gna_tiled_elems(B, heads, dims, head_dim, tile)),
-                out=(out, nr), lse=(lse, nr // head_dim), descale=(descale, 3))
-    opt = GNAOptions()
-    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
-    opt.leader_rule = leader_rule
-    opt.scale = scale
-    opt.descale = _ptr(descale)
+    nkv = gna_tiled_elems(B, heads, dims, head_dim, tile_kv if tile_kv is not None else tile)
+    dev = _need(q=(q, nr), k=(k, nr), v_value=(v_value, nkv), out=(out, nr), lse=(lse, nr // head_dim),
+                descale=(descale, 3))
+    opt = _options(tile, leader_rule, scale, descale, tile_kv)
     _check(lib().gna_forward_raster(_ptr(q), _ptr(k), _ptr(v_value), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                     _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
                                     _stream_ptr(stream, dev)))
@@ -382,7 +393,8 @@ def gna_forward_raster(q: torch.Tensor, k: torch.Tensor, v_value: torch.Tensor, 
 
 def gna_forward_raster_all(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
                            lse: torch.Tensor | None, B: int, heads: int, dims, window, stride, head_dim: int, *,
-                           tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, stream=None):
+                           tile=None, leader_rule: int = GNA_LEADER_CENTER, scale: float = 0.0, tile_kv=None,
+                           stream=None):
     """GNA forward with every tensor in the raster layout (see ``include/gna.h``):
     q, k, v bf16 ``[B, T, H, W, heads, 128]``, ``out`` bf16 raster, ``lse`` float32
     ``[B, T, H, W, heads]`` or None.  No permute; slower P V than
@@ -396,10 +408,7 @@ def gna_forward_raster_all(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, ou
         raise ValueError("lse must be float32")
     nr = _raster_elems(B, heads, dims, head_dim)
     dev = _need(q=(q, nr), k=(k, nr), v=(v, nr), out=(out, nr), lse=(lse, nr // head_dim))
-    opt = GNAOptions()
-    opt.tile = (ctypes.c_int * 3)(*(tile or (0, 0, 0)))
-    opt.leader_rule = leader_rule
-    opt.scale = scale
+    opt = _options(tile, leader_rule, scale, None, tile_kv)
     _check(lib().gna_forward_raster_all(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, heads, _I3(*dims),
                                         _I3(*window), _I3(*stride), head_dim, code, ctypes.byref(opt),
                                         _stream_ptr(stream, dev)))
@@ -499,12 +508,17 @@ def gna_schedule_step(step: int, num_steps: int, full_steps: int, dims, window, 
     return tuple(w), tuple(s_)
 
 
-def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADER_CENTER):
-    """(visited KV tiles, KV tiles needing the element mask, Q tiles) of one (b, head) plane."""
+def gna_tile_stats(dims, window, stride, tile=None, leader_rule: int = GNA_LEADER_CENTER, *, tile_kv=None):
+    """(visited KV tiles, KV tiles needing the element mask, Q tiles) of one (b, head) plane;
+    with ``tile_kv`` (``gna_tile_stats_qkv``) the KV tiles have their own shape."""
     v, p_, q = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
     t = None if tile is None else ctypes.cast(_I3(*tile), _P)
-    _check(lib().gna_tile_stats(_I3(*dims), _I3(*window), _I3(*stride), t, leader_rule,
-                                ctypes.byref(v), ctypes.byref(p_), ctypes.byref(q)))
+    if tile_kv is None:
+        _check(lib().gna_tile_stats(_I3(*dims), _I3(*window), _I3(*stride), t, leader_rule,
+                                    ctypes.byref(v), ctypes.byref(p_), ctypes.byref(q)))
+    else:
+        _check(lib().gna_tile_stats_qkv(_I3(*dims), _I3(*window), _I3(*stride), t, ctypes.cast(_I3(*tile_kv), _P),
+                                        leader_rule, ctypes.byref(v), ctypes.byref(p_), ctypes.byref(q)))
     return v.value, p_.value, q.value
 
 
@@ -516,6 +530,16 @@ def gna_plan_tile(dims, window, stride, leader_rule: int = GNA_LEADER_CENTER):
     _check(lib().gna_plan_tile(_I3(*dims), _I3(*window), _I3(*stride), leader_rule, t, ctypes.byref(ov),
                                ctypes.byref(sp)))
     return tuple(t), ov.value, sp.value
+
+
+def gna_plan_tiles(dims, window, stride, leader_rule: int = GNA_LEADER_CENTER):
+    """(tile_q, tile_kv, tile_overhead, speedup_bound): the query and key/value tiles,
+    chosen independently, with the fewest visited 128 x 128 tile pairs."""
+    tq, tk = _I3(), _I3()
+    ov, sp = ctypes.c_double(), ctypes.c_double()
+    _check(lib().gna_plan_tiles(_I3(*dims), _I3(*window), _I3(*stride), leader_rule, tq, tk, ctypes.byref(ov),
+                                ctypes.byref(sp)))
+    return tuple(tq), tuple(tk), ov.value, sp.value
 
 
 def gna_permuted_elems(B: int, heads: int, dims, head_dim: int) -> int:

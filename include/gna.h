@@ -103,6 +103,14 @@ typedef struct {
                              per-tensor dequantisation scales of q, k, v (value =
                              code * descale); required (pass 1, 1, 1 explicitly for
                              unscaled codes).  Must be NULL for GNA_BF16.           */
+    int tile_kv[3];       /* forward only: tile of k and v when it differs from the
+                             tile of q, out and lse (GNA page §1.2: query and
+                             key/value tiles sized independently); {0,0,0} = the
+                             same tile as q.  Both are 128-element power-of-two
+                             tiles; k and v are then permuted with tile_kv (the
+                             *_tiled permutes), q, out and lse with `tile`.
+                             gna_plan_tiles picks a pair.  The backward pass
+                             needs the two equal (GNA_ERR_UNSUPPORTED).          */
 } gna_options;
 
 /* ------------------------------------------------------------ layout ---- */
@@ -192,8 +200,10 @@ gna_status gna_forward_fp8(const void* q, const void* k, const void* v_value, vo
                            int B, int heads, const int dims[3], const int window[3], const int stride[3],
                            int head_dim, const float* descale_qkv, void* stream);
 
-/* gna_forward with explicit options (tile, leader rule, scale, fp8 descales),
- * for either dtype; GNA_FP8_E4M3 requires opt->descale. */
+/* gna_forward with explicit options (tile, leader rule, scale, fp8 descales,
+ * a separate key/value tile), for either dtype; GNA_FP8_E4M3 requires
+ * opt->descale.  With opt->tile_kv set, q, out and lse are tiled with
+ * opt->tile and k, v_value with opt->tile_kv (sizes gna_tiled_elems of each). */
 gna_status gna_forward_ex(const void* q, const void* k, const void* v_value, void* out, float* lse,
                           int B, int heads, const int dims[3], const int window[3], const int stride[3],
                           int head_dim, gna_dtype dtype, const gna_options* opt, void* stream);
@@ -203,11 +213,12 @@ gna_status gna_forward_ex(const void* q, const void* k, const void* v_value, voi
  * a view of the token grid); the kernel gathers each 128-token Q and K tile
  * straight from the raster tensors, a 5-D TMA box for K and row loads for Q,
  * and writes O and lse back to raster rows.  Query rows of padded tile slots
- * are neither read nor written.
+ * are neither read nor written.  opt->tile_kv, if set, shapes the K boxes and
+ * the value layout of v_value; opt->tile the query tiles.
  *
  * q, k    : raster [B, T, H, W, heads, head_dim], row stride heads*head_dim
  * v_value : value layout [B, heads, tiles, head_dim, 128] (gna_permute_v_tiled
- *           with the same tile; not raster)
+ *           with the key/value tile; not raster)
  * out     : raster [B, T, H, W, heads, head_dim] bfloat16
  * lse     : raster [B, T, H, W, heads] float32, natural log; may be NULL
  * Everything else as gna_forward_ex; opt may be NULL.  All pointers 16-byte
@@ -321,6 +332,15 @@ gna_status gna_tile_stats(const int dims[3], const int window[3], const int stri
                           const int tile[3], int leader_rule,
                           int64_t* visited_kv_tiles, int64_t* partial_kv_tiles, int64_t* q_tiles);
 
+/* gna_tile_stats for query tiles `tile_q` and key/value tiles `tile_kv` (NULL =
+ * default tile for either): the KV tiles, in units of tile_kv, that the
+ * windows of each Q tile reach, and how many of them need the mask; q_tiles
+ * counts tile_q tiles.  gna_tile_stats(..., tile, ...) is this call with
+ * tile_q = tile_kv = tile.  Host only. */
+gna_status gna_tile_stats_qkv(const int dims[3], const int window[3], const int stride[3], const int tile_q[3],
+                              const int tile_kv[3], int leader_rule, int64_t* visited_kv_tiles,
+                              int64_t* partial_kv_tiles, int64_t* q_tiles);
+
 /* Tile planner: the analytic speedup bound the GNA page suggests checking before
  * deployment (§4.2, problem 2; a NATTENSim-like count).  Over every 128-element
  * power-of-two tile it counts, with gna_tile_stats, the 128 x 128 tiles the
@@ -335,6 +355,15 @@ gna_status gna_tile_stats(const int dims[3], const int window[3], const int stri
  * Host only.  GNA_ERR_INVALID_ARG on bad geometry or leader rule. */
 gna_status gna_plan_tile(const int dims[3], const int window[3], const int stride[3], int leader_rule,
                          int tile[3], double* tile_overhead, double* speedup_bound);
+
+/* gna_plan_tile over pairs: query tile and key/value tile chosen independently
+ * (GNA page §1.2, decoupled Q and KV tiles) among all 128-element power-of-two
+ * tiles, fewest visited 128 x 128 tile pairs first, then fewest partial ones,
+ * then equal tiles (the default tile preferred).  speedup_bound = the Q tiles
+ * x KV tiles of dense attention on this tiling / the visited pairs.  Host
+ * only; errors as gna_plan_tile. */
+gna_status gna_plan_tiles(const int dims[3], const int window[3], const int stride[3], int leader_rule,
+                          int tile_q[3], int tile_kv[3], double* tile_overhead, double* speedup_bound);
 
 /* Step schedule of a diffusion sampler.  The GNA page keeps full attention for
  * the first steps and switches to GNA afterwards: §3.2 runs the first 9 of 28

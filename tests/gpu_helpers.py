@@ -35,25 +35,28 @@ def oracle_threads() -> int:
 
 
 def gpu_gna(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, dims, window, stride, *, tile=None,
-            leader_rule=G.GNA_LEADER_CENTER, scale=0.0, descale=None):
+            leader_rule=G.GNA_LEADER_CENTER, scale=0.0, descale=None, tile_kv=None):
     """Raster CPU tensors [B, T, H, W, heads, d] -> (out raster float32 [.., d], lse raster [.., heads]).
 
     Uploads, permutes (q, k tiled; v into the value layout), runs the forward,
-    unpermutes out and lse, downloads.
+    unpermutes out and lse, downloads.  With ``tile_kv``, k and v are permuted
+    with that tile and q, out, lse with ``tile``.
     """
     B, T, H, W, heads, d = q.shape
     dev = torch.device("cuda")
+    tkv = tile_kv if tile_kv is not None else tile
     shp = G.tiled_shape(B, heads, dims, d, tile)
-    qt, kt = (torch.empty(shp, dtype=x.dtype, device=dev) for x in (q, k))
-    vt = torch.empty(G.value_shape(B, heads, dims, d, tile), dtype=v.dtype, device=dev)
-    for src, dst in ((q, qt), (k, kt)):
-        G.gna_permute(src.to(dev).contiguous(), dst, B, heads, dims, d, tile=tile)
-    G.gna_permute_v(v.to(dev).contiguous(), vt, B, heads, dims, d, tile=tile)
+    qt = torch.empty(shp, dtype=q.dtype, device=dev)
+    kt = torch.empty(G.tiled_shape(B, heads, dims, d, tkv), dtype=k.dtype, device=dev)
+    vt = torch.empty(G.value_shape(B, heads, dims, d, tkv), dtype=v.dtype, device=dev)
+    G.gna_permute(q.to(dev).contiguous(), qt, B, heads, dims, d, tile=tile)
+    G.gna_permute(k.to(dev).contiguous(), kt, B, heads, dims, d, tile=tkv)
+    G.gna_permute_v(v.to(dev).contiguous(), vt, B, heads, dims, d, tile=tkv)
     out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
     lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     ds = None if descale is None else torch.tensor(descale, dtype=torch.float32, device=dev)
     G.gna_forward(qt, kt, vt, out_t, lse_t, B, heads, dims, window, stride, d, tile=tile,
-                  leader_rule=leader_rule, scale=scale, descale=ds)
+                  leader_rule=leader_rule, scale=scale, descale=ds, tile_kv=tile_kv)
     out = torch.empty((B,) + tuple(dims) + (heads, d), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B,) + tuple(dims) + (heads, 1), dtype=torch.float32, device=dev)
     G.gna_unpermute(out_t, out, B, heads, dims, d, tile=tile)

@@ -192,8 +192,10 @@ def test_tiled_elems(L):
     assert G.tiled_shape(1, 2, (1, 16, 16), 32) == (1, 2, 2, 128, 32)
 
 
-def _brute_tile_stats(dims, window, stride, tile, rule):
-    """Count, by enumerating queries and keys, the KV tiles each Q tile visits."""
+def _brute_tile_stats(dims, window, stride, tile, rule, tile_kv=None):
+    """Count, by enumerating queries and keys, the KV tiles (of shape ``tile_kv``,
+    default ``tile``) each Q tile (of shape ``tile``) visits."""
+    tkv = tile if tile_kv is None else tile_kv
     nt = [-(-L // t) for L, t in zip(dims, tile)]
     starts = [[ref.window_start(i, L, w, s, rule) for i in range(L)] for L, w, s in zip(dims, window, stride)]
     visited = partial = 0
@@ -208,10 +210,10 @@ def _brute_tile_stats(dims, window, stride, tile, rule):
             touched = {}
             for i in range(q_lo[d], q_hi[d] + 1):
                 for j in range(starts[d][i], starts[d][i] + window[d]):
-                    touched[j // tile[d]] = True
+                    touched[j // tkv[d]] = True
             full = {}
             for kt in touched:
-                pos = range(kt * tile[d], kt * tile[d] + tile[d])
+                pos = range(kt * tkv[d], kt * tkv[d] + tkv[d])
                 full[kt] = all(starts[d][i] <= j < starts[d][i] + window[d]
                                for i in range(q_lo[d], q_hi[d] + 1) for j in pos)
             per_dim.append(full)
@@ -232,6 +234,64 @@ def _brute_tile_stats(dims, window, stride, tile, rule):
 def test_tile_stats_match_brute_force(L, dims, window, stride, tile, rule):
     code = 0 if rule == ref.LEADER_CENTER else 1
     assert G.gna_tile_stats(dims, window, stride, tile, code) == _brute_tile_stats(dims, window, stride, tile, rule)
+
+
+@pytest.mark.parametrize("dims,window,stride,tile,tile_kv", [
+    ((6, 20, 24), (4, 9, 8), (2, 3, 8), (2, 8, 8), (4, 4, 8)),
+    ((5, 24, 40), (3, 7, 9), (1, 2, 3), (1, 8, 16), (2, 4, 16)),
+    ((3, 5, 7), (2, 3, 4), (2, 2, 3), (2, 8, 8), (1, 4, 32)),
+    ((1, 37, 45), (1, 11, 13), (1, 1, 1), (1, 8, 16), (1, 16, 8)),
+    ((8, 16, 16), (4, 8, 8), (4, 8, 8), (4, 4, 8), (2, 8, 8)),
+])
+def test_tile_stats_decoupled_match_brute_force(L, dims, window, stride, tile, tile_kv):
+    """Q and KV tiles of different shapes (GNA page §1.2): the visited KV tiles, in
+    units of the KV tile, and the partial ones, against enumeration."""
+    for rule, code in ((ref.LEADER_CENTER, 0), (ref.LEADER_LITERAL, 1)):
+        got = G.gna_tile_stats(dims, window, stride, tile, code, tile_kv=tile_kv)
+        assert got == _brute_tile_stats(dims, window, stride, tile, rule, tile_kv=tile_kv)
+    # equal tiles: the single-tile call
+    assert G.gna_tile_stats(dims, window, stride, tile, tile_kv=tile) == G.gna_tile_stats(dims, window, stride, tile)
+
+
+@pytest.mark.parametrize("dims,window,stride", [
+    ((30, 48, 80), (16, 32, 48), (8, 8, 8)),
+    ((30, 48, 80), (16, 32, 48), (16, 8, 8)),
+    ((30, 48, 80), (16, 32, 48), (1, 1, 1)),
+    ((6, 20, 24), (4, 9, 8), (2, 3, 8)),
+])
+def test_plan_tiles_is_the_minimum_over_all_pairs(L, dims, window, stride):
+    """The pair planner visits no more tile pairs than any (Q tile, KV tile) pair,
+    never more than the best single tile, and keeps equal tiles unless a pair
+    does strictly better; its ratios follow from the counts."""
+    tiles = [(1 << a, 1 << b, 1 << (7 - a - b)) for a in range(8) for b in range(8 - a)]
+    counts = {(tq, tk): G.gna_tile_stats(dims, window, stride, tq, tile_kv=tk)[:2] for tq in tiles for tk in tiles}
+    tq, tk, overhead, speedup = G.gna_plan_tiles(dims, window, stride)
+    best = min(counts.values())
+    assert counts[(tq, tk)] == best
+    single, single_overhead, _ = G.gna_plan_tile(dims, window, stride)
+    if best == counts[(single, single)]:
+        assert tq == tk == single
+    assert overhead <= single_overhead
+    useful = np.prod(dims) * np.prod(window)
+    assert math.isclose(overhead, best[0] * 128 * 128 / useful, rel_tol=1e-12)
+    nq = np.prod([-(-L_ // t_) for L_, t_ in zip(dims, tq)])
+    nk = np.prod([-(-L_ // t_) for L_, t_ in zip(dims, tk)])
+    assert math.isclose(speedup, nq * nk / best[0], rel_tol=1e-12)
+
+
+def test_decoupled_tiles_validated_on_host(L):
+    """A bad key/value tile is refused before any launch; the backward pass refuses
+    a key/value tile that differs from the query tile."""
+    geom = (1, 2, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1))
+    opt = G.GNAOptions()
+    opt.tile_kv = (ctypes.c_int * 3)(1, 8, 8)          # 64 elements
+    assert L.gna_forward_ex(FAKE, FAKE, FAKE, FAKE, None, *geom, 32, G.GNA_BF16, ctypes.byref(opt),
+                            None) == G.GNA_ERR_INVALID_ARG
+    opt.tile_kv = (ctypes.c_int * 3)(1, 4, 32)
+    args = (FAKE,) * 8 + (1, 2, I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1), 128, G.GNA_BF16, ctypes.byref(opt), None)
+    assert L.gna_backward_dq(*args) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_backward_dkdv(*args) == G.GNA_ERR_UNSUPPORTED
+    assert "key/value tile" in L.gna_last_error().decode()
 
 
 def test_blocked_window_aligned_with_tiles_needs_no_mask(L):
