@@ -70,6 +70,8 @@ def parse_args(argv=None):
                     help="also run the forward back to back for this many seconds and report the sustained rate")
     ap.add_argument("--backward", action="store_true",
                     help="also time the backward pass (delta, dq, dk/dv kernels; bf16, head_dim 128, tiled layout)")
+    ap.add_argument("--measure-host-link", action="store_true",
+                    help="only measure the pinned host <-> device copy rate of the end-to-end step's sizes")
     ap.add_argument("--measure-e4m3-gemm", action="store_true",
                     help="only time a dense e4m3 GEMM (torch._scaled_mm, 8192^3, bf16 out) as a burst and "
                          "for 4 s back to back, print one JSON line and exit")
@@ -123,6 +125,43 @@ def load_e4m3_peak():
         return float(rec["e4m3_tflops"]), float(rec["e4m3_tflops_sustained"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def measure_host_link(h2d_bytes: int = 2123366400, d2h_bytes: int = 718848000, reps: int = 5) -> dict:
+    """The host link the end-to-end figure rides on: one pinned host -> device copy
+    of the bench step's upload size alone, and the same with a device -> host copy
+    of the step's download size running concurrently on another stream (CUDA events,
+    best of `reps`)."""
+    dev = torch.device("cuda")
+    h = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    ho = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    do = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def timed(both: bool) -> float:
+        best = float("inf")
+        for _ in range(reps + 1):
+            torch.cuda.synchronize()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(s_in)
+            s_out.wait_event(e0)
+            with torch.cuda.stream(s_in):
+                d.copy_(h, non_blocking=True)
+            e1.record(s_in)
+            if both:
+                with torch.cuda.stream(s_out):
+                    ho.copy_(do, non_blocking=True)
+            e2.record(s_out)
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return best
+
+    alone, with_down = timed(False), timed(True)
+    return {"h2d_gbs_alone": h2d_bytes / (alone / 1e3) / 1e9, "h2d_gbs_with_d2h": h2d_bytes / (with_down / 1e3) / 1e9,
+            "h2d_bytes": h2d_bytes, "d2h_bytes": d2h_bytes,
+            "how": f"pinned host -> device copy of the step's upload size, alone and with a device -> host copy of "
+                   f"the step's download size on another stream; best of {reps}, CUDA events"}
 
 
 def measure_e4m3_gemm(n: int = 8192, seconds: float = 4.0) -> dict:
@@ -736,6 +775,9 @@ def gpu_arm(a, rank, world, local):
 
 def main(argv=None):
     a = parse_args(argv)
+    if a.measure_host_link:
+        print(json.dumps(measure_host_link()), flush=True)
+        return
     if a.measure_e4m3_gemm:
         print(json.dumps(measure_e4m3_gemm()), flush=True)
         return
