@@ -11,7 +11,11 @@
 // softmax is accumulated block by block and the n x n matrix never exists.
 //
 // One CTA owns one 128-query tile of one (batch, head) and walks the box of
-// KV tiles its windows touch.  Warp roles (320 threads):
+// KV tiles its windows touch.  Query tiles (q, out, lse) and key/value tiles
+// (k, v) are both 128-token boxes of the grid, of the same shape or, as the GNA
+// page's §1.2 allows, of two different shapes; the KV box, the element mask and
+// the K / V loads use the KV tile, the query rows the query tile.  Warp roles
+// (320 threads):
 //   warp 0      TMA producer: K and V tiles through NS-stage mbarrier rings
 //   warp 1      TMEM allocator and tcgen05.mma issuer (lane 0)
 //   warps 2..9  softmax / correction / epilogue.  Thread = (query row, half):
