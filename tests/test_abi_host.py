@@ -88,7 +88,7 @@ def test_forward_ex_rejects_bad_options(L):
         assert L.gna_forward_ex(*args, ctypes.byref(opt), None) == G.GNA_ERR_INVALID_ARG
 
 
-def test_survey_boundary_calls_exist_and_validate_on_host(L):
+def test_boundary_calls_exist_and_validate_on_host(L):
     """Every call of the planned C ABI is exported under its name and checks its
     arguments before launching anything."""
     for name in ("gna_forward", "gna_forward_fp8", "gna_permute", "gna_unpermute", "gna_tile_shape",
