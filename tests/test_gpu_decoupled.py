@@ -44,6 +44,20 @@ def test_decoupled_small_grids_all_queries(d, dims, window, stride, tile, tile_k
     assert rel < REL_RMS_BF16, info
 
 
+def test_decoupled_literal_leader_rule_and_scale():
+    """The pair with the literal leader offset (GNA_LEADER_LITERAL) and a custom
+    softmax scale, every query against the oracle."""
+    dims, window, stride, d, B, heads = (6, 20, 24), (4, 8, 8), (2, 4, 4), 64, 1, 2
+    q, k, v = bf16_inputs(9350, B, dims, heads, d)
+    out, lse = gpu_gna(q, k, v, dims, window, stride, tile=(2, 8, 8), tile_kv=(2, 4, 16),
+                       leader_rule=G.GNA_LEADER_LITERAL, scale=0.2)
+    o_ref, l_ref = oracle.forward_c(exact_f32(q), exact_f32(k), exact_f32(v), dims, window, stride,
+                                    rule=oracle.LEADER_LITERAL, scale=0.2, threads=oracle_threads())
+    rel, info = compare(out, lse, o_ref, l_ref, TOL_BF16_OUT, TOL_BF16_LSE, dims=list(dims), window=list(window),
+                        stride=list(stride), heads=heads, B=B, head_dim=d)
+    assert rel < REL_RMS_BF16, info
+
+
 def test_decoupled_equal_tiles_match_the_single_tile_call():
     """tile_kv equal to the tile is the single-tile call: bit-identical output."""
     dims, window, stride, d = (6, 20, 24), (4, 9, 8), (2, 3, 8), 64
