@@ -361,7 +361,11 @@ gna_status gna_plan_tile(const int dims[3], const int window[3], const int strid
  * tiles, fewest visited 128 x 128 tile pairs first, then fewest partial ones,
  * then equal tiles (the default tile preferred).  speedup_bound = the Q tiles
  * x KV tiles of dense attention on this tiling / the visited pairs.  Host
- * only; errors as gna_plan_tile. */
+ * only; errors as gna_plan_tile.  The count is all it weighs: the forward
+ * kernel has the element mask of KV tiles 2x8x8 and 1x8x16 (at head_dim 128
+ * also 2x4x16 and 4x4x8) compiled in and runs any other KV tile with a
+ * generic, slower mask, so a pair that saves only a few percent of the tile
+ * pairs with another KV tile may run slower than the default tile. */
 gna_status gna_plan_tiles(const int dims[3], const int window[3], const int stride[3], int leader_rule,
                           int tile_q[3], int tile_kv[3], double* tile_overhead, double* speedup_bound);
 
