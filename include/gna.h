@@ -53,6 +53,11 @@
  *   nothing per call.
  * * `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Calls enqueue work and return GNA_OK without synchronising.
+ *   Apart from gna_get_status (which synchronises), every call may be
+ *   captured into a CUDA graph once it has been made on the device outside a
+ *   capture (the first call sets kernel attributes and, for
+ *   gna_backward_noalloc, looks up its workspace); a replay reads the
+ *   captured buffers' current contents.
  * * Argument errors are detected on the host before anything is enqueued and
  *   return GNA_ERR_INVALID_ARG / GNA_ERR_UNSUPPORTED; nothing is launched.
  *   Launch failures return GNA_ERR_CUDA.  gna_last_error() gives a message.
