@@ -695,8 +695,8 @@ gna_status backward_common(int B, int heads, const int dims[3], const int window
     if (B < 1 || heads < 1) return fail(GNA_ERR_INVALID_ARG, "B and heads must be >= 1");
     gna_status st = check_geometry(dims, window, stride);
     if (st != GNA_OK) return st;
-    if (dtype != GNA_BF16 || head_dim != 128)
-        return fail(GNA_ERR_UNSUPPORTED, "the backward pass supports bf16 with head_dim 128");
+    if (dtype != GNA_BF16 || (head_dim != 64 && head_dim != 128))
+        return fail(GNA_ERR_UNSUPPORTED, "the backward pass supports bf16 with head_dim 64 or 128");
     const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
     if (rule != GNA_LEADER_CENTER && rule != GNA_LEADER_LITERAL)
         return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", rule);
@@ -728,7 +728,8 @@ gna_status gna_backward_delta(const void* out, const void* dout, float* delta, i
     int64_t nq = 0;
     gna_status st = backward_common(B, heads, dims, dims, dims, head_dim, dtype, opt, tile, tlog, &nq);
     if (st != GNA_OK) return st;
-    cudaError_t e = gna::launch_backward_delta(out, dout, delta, nq * gna::kTileElems, static_cast<cudaStream_t>(stream));
+    cudaError_t e = gna::launch_backward_delta(out, dout, delta, nq * gna::kTileElems, head_dim,
+                                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward delta launch");
     t_last_error.clear();
     return GNA_OK;
@@ -771,7 +772,7 @@ gna_status gna_backward_dkdv(const void* q, const void* k, const void* v, const 
     if ((st = make_tile_map(&p.tmDO, dout, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_tile_map(&p.tmK, k, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_tile_map(&p.tmV, v, rows, head_dim, 2)) != GNA_OK) return st;
-    cudaError_t e = gna::launch_backward_dkdv(p, nt_all, static_cast<cudaStream_t>(stream));
+    cudaError_t e = gna::launch_backward_dkdv(p, head_dim, nt_all, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward dk/dv launch");
     t_last_error.clear();
     return GNA_OK;
@@ -816,7 +817,7 @@ gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, co
     if ((st = make_tile_map(&p.tmK, k, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_tile_map(&p.tmV, v, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_value_map(&p.tmKv, k_value, nq, head_dim, 2)) != GNA_OK) return st;
-    cudaError_t e = gna::launch_backward_dq(p, nq, static_cast<cudaStream_t>(stream));
+    cudaError_t e = gna::launch_backward_dq(p, head_dim, nq, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward dq launch");
     t_last_error.clear();
     return GNA_OK;

@@ -55,15 +55,32 @@ constexpr uint32_t kColDO = 448;
 constexpr int kBStages = 2;
 constexpr float kBLog2e = 1.4426950408889634f;
 
-// bf16, head_dim 128
-constexpr int kD = 128;
-constexpr int kRowBytes = kD * 2;                  // 256 B per token row
-constexpr int kTileBytes = kTileElems * kRowBytes; // 32 KB per 128-token tile
-constexpr int kStageBytes = 3 * kTileBytes;        // K, V, K (value layout)
-constexpr int kSmemAlloc = kStageBytes * kBStages + 1024;
-constexpr int kQKSteps = kRowBytes / 32;           // K = 16 bf16 per MMA
-constexpr int kDQSteps = kTileElems / 16;
+constexpr int kDQSteps = kTileElems / 16;        // K = 16 bf16 per MMA over 128 keys / queries
 constexpr uint32_t kIdesc = make_idesc(128, 128, kFmtBF16, false);
+
+// bf16 tiles of head_dim D (64 or 128): a token row is 2 D bytes, one or two
+// 128-byte swizzle spans
+template <int D>
+struct BwdCfg {
+    static constexpr int kRowBytes = D * 2;                    // bytes per token row
+    static constexpr int kChunks = kRowBytes / 128;            // 128-byte spans per row (TMA boxes per tile)
+    static constexpr int kTileBytes = kTileElems * kRowBytes;  // one 128-token tile
+    static constexpr int kStageBytes = 3 * kTileBytes;         // K, V, K (value layout)
+    // at least ~116 KB, so that one CTA (which takes all 512 TMEM columns) is
+    // resident per SM and a second one never waits in the TMEM allocation
+    static constexpr int kMinSmem = 118784;
+    static constexpr int kSmemAlloc = (kStageBytes * kBStages + 1024) > kMinSmem ? (kStageBytes * kBStages + 1024)
+                                                                                 : kMinSmem;
+    static constexpr int kQKSteps = kRowBytes / 32;            // MMA k-steps over the head dimension
+    static constexpr int kHalfWords = kRowBytes / 8;           // TMEM columns of half a Q / dO row
+    static constexpr int kHalfPieces = D / 64;                 // 32-column pieces of half a dQ / dK / dV row
+    static constexpr uint32_t kIdescDQ = make_idesc(128, D, kFmtBF16, false);    // dQ += dS K: N = D
+    static constexpr int kKVStageBytes = 2 * kTileBytes + 1024;                  // Q_i, dO_i, lse_i, delta_i
+    static constexpr int kKVSmemAlloc = (2 * kTileBytes + kBStages * kKVStageBytes + 1024) > kMinSmem
+                                            ? (2 * kTileBytes + kBStages * kKVStageBytes + 1024) : kMinSmem;
+    static constexpr uint32_t kIdescMN = make_idesc(128, D, kFmtBF16, true);     // dV, dK: N = D, B MN-major
+    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+};
 
 struct BwdBars {
     uint64_t qdo_full;            // Q and dO rows stored in TMEM (8 warps)
@@ -140,6 +157,18 @@ __device__ __forceinline__ float2 bwd_fmul2(float2 a, float2 b)
     return d;
 }
 
+// N = 16 or 32 consecutive TMEM columns of this warp's lane quarter
+template <int N>
+__device__ __forceinline__ void bwd_tmem_st(uint32_t taddr, const uint32_t (&r)[N])
+{
+    if constexpr (N == 32) {
+        tmem_st32(taddr, r);
+    } else {
+        static_assert(N == 16, "16 or 32 columns");
+        tmem_st16(taddr, r);
+    }
+}
+
 template <int N>
 __device__ __forceinline__ void bwd_reg_fence(uint32_t (&r)[N])
 {
@@ -149,8 +178,10 @@ __device__ __forceinline__ void bwd_reg_fence(uint32_t (&r)[N])
                      "+r"(r[i + 6]), "+r"(r[i + 7]));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_constant__ BwdParams p)
 {
+    using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ BwdBars bars;
@@ -226,17 +257,20 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             }
             if (j == p.fault_skip_kv) { early = true; break; }   // test hook: consumers wait in vain
             if (elect_one_sync()) {
-                const uint32_t st = s_base + s * kStageBytes;
-                mbar_arrive_expect_tx(bar(bars.full[s]), kStageBytes);
+                const uint32_t st = s_base + s * C::kStageBytes;
+                mbar_arrive_expect_tx(bar(bars.full[s]), C::kStageBytes);
                 const int32_t row = static_cast<int32_t>(tile * kTileElems);
-                const int32_t vrow = static_cast<int32_t>(tile * kD);
+                const int32_t vrow = static_cast<int32_t>(tile * D);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < C::kChunks; ++c) {
                     // K and V tiles: 128 rows x 64 elements per box (128-byte swizzle)
                     tma_load_2d(st + c * kTileElems * 128, &p.tmK, bar(bars.full[s]), c * 64, row);
-                    tma_load_2d(st + kTileBytes + c * kTileElems * 128, &p.tmV, bar(bars.full[s]), c * 64, row);
+                    tma_load_2d(st + C::kTileBytes + c * kTileElems * 128, &p.tmV, bar(bars.full[s]), c * 64, row);
+                }
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
                     // K in the value layout: d rows x 64 tokens per box
-                    tma_load_2d(st + 2 * kTileBytes + c * kD * 128, &p.tmKv, bar(bars.full[s]), c * 64, vrow);
+                    tma_load_2d(st + 2 * C::kTileBytes + c * D * 128, &p.tmKv, bar(bars.full[s]), c * 64, vrow);
                 }
             }
             __syncwarp();
@@ -260,10 +294,10 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (j / kBStages) & 1, &abort_flag, &g_bwd_status)))
                 return false;
             tc_fence_after();
-            const uint64_t dK = d0 + static_cast<uint64_t>((s * kStageBytes) >> 4);
+            const uint64_t dK = d0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
             if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < kQKSteps; ++kk) {
+                for (int kk = 0; kk < C::kQKSteps; ++kk) {
                     // k-step kk: features [16 kk, 16 kk + 16) = 32 bytes of every token row
                     const int off = ((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128);
                     mma_f16_ts(tS, tQ + kk * 8, dK + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
@@ -275,10 +309,10 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         };
         auto issue_dp = [&](int j) {       // K/V of tile j landed (issue_s(j) waited for them)
             const int s = j % kBStages;
-            const uint64_t dV = d0 + static_cast<uint64_t>((s * kStageBytes + kTileBytes) >> 4);
+            const uint64_t dV = d0 + static_cast<uint64_t>((s * C::kStageBytes + C::kTileBytes) >> 4);
             if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < kQKSteps; ++kk) {
+                for (int kk = 0; kk < C::kQKSteps; ++kk) {
                     const int off = ((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128);
                     mma_f16_ts(tDP, tDO + kk * 8, dV + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
                 }
@@ -311,15 +345,15 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
                 break;
             }
             tc_fence_after();
-            const uint64_t dKv = d0 + static_cast<uint64_t>((s * kStageBytes + 2 * kTileBytes) >> 4);
+            const uint64_t dKv = d0 + static_cast<uint64_t>((s * C::kStageBytes + 2 * C::kTileBytes) >> 4);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kDQSteps; ++kk) {
                     // k-step kk: key columns [16 kk, 16 kk + 16); dS of key column
                     // half h sits at the front of dP columns [64 h, 64 h + 64)
                     const uint32_t a = tDP + (kk >> 2) * 64 + (kk & 3) * 8;
-                    const int off = ((kk * 32) / 128) * (kD * 128) + ((kk * 32) % 128);
-                    mma_f16_ts(tDQ, a, dKv + static_cast<uint64_t>(off >> 4), kIdesc, (j > 0 || kk > 0) ? 1u : 0u);
+                    const int off = ((kk * 32) / 128) * (D * 128) + ((kk * 32) % 128);
+                    mma_f16_ts(tDQ, a, dKv + static_cast<uint64_t>(off >> 4), C::kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
                 }
                 mma_commit(bar(bars.empty[s]));
                 if (j == n_kv - 1) mma_commit(bar(bars.dq_final));
@@ -359,23 +393,24 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
 
         // this half of the Q and dO rows -> TMEM (A operands of S and dP)
         {
-            const uint4* qs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + grow * kRowBytes +
-                                                             half * (kRowBytes / 2));
+            constexpr int W = C::kHalfWords;
+            const uint4* qs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + grow * C::kRowBytes +
+                                                             half * (C::kRowBytes / 2));
             const uint4* ds = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.dout) +
-                                                             grow * kRowBytes + half * (kRowBytes / 2));
-            uint32_t w[32];
+                                                             grow * C::kRowBytes + half * (C::kRowBytes / 2));
+            uint32_t w[W];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < W / 4; ++i) {
                 const uint4 v = __ldg(qs + i);
                 w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
             }
-            tmem_st32(tmem + kColQ + lane_addr + half * 32, w);
+            bwd_tmem_st<W>(tmem + kColQ + lane_addr + half * W, w);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < W / 4; ++i) {
                 const uint4 v = __ldg(ds + i);
                 w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
             }
-            tmem_st32(tmem + kColDO + lane_addr + half * 32, w);
+            bwd_tmem_st<W>(tmem + kColDO + lane_addr + half * W, w);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -465,11 +500,11 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         }
         if (ok) {
             tc_fence_after();
-            uint8_t* dst_row = static_cast<uint8_t*>(p.dq) + grow * kRowBytes + half * (kRowBytes / 2);
+            uint8_t* dst_row = static_cast<uint8_t*>(p.dq) + grow * C::kRowBytes + half * (C::kRowBytes / 2);
 #pragma unroll
-            for (int pc = 0; pc < 2; ++pc) {
+            for (int pc = 0; pc < C::kHalfPieces; ++pc) {
                 uint32_t r[32];
-                tmem_ld32(tmem + kColDQ + lane_addr + half * 64 + pc * 32, r);
+                tmem_ld32(tmem + kColDQ + lane_addr + half * (D / 2) + pc * 32, r);
                 tmem_wait_ld();
                 bwd_reg_fence(r);
                 uint32_t pk[16];
@@ -518,9 +553,6 @@ constexpr uint32_t kColDV = 0;
 constexpr uint32_t kColDK = 128;
 constexpr uint32_t kColST = 256;
 constexpr uint32_t kColDPT = 384;
-constexpr int kKVStageBytes = 2 * kTileBytes + 1024;            // Q_i, dO_i, lse_i, delta_i (1024-aligned)
-constexpr int kKVSmemAlloc = 2 * kTileBytes + kBStages * kKVStageBytes + 1024;
-constexpr uint32_t kIdescMN = make_idesc(128, 128, kFmtBF16, true);
 
 struct KVBars {
     uint64_t kv_full;             // K_j and V_j landed
@@ -534,8 +566,10 @@ struct KVBars {
     uint64_t drain;
 };
 
+template <int D>
 __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid_constant__ BwdKVParams p)
 {
+    using C = BwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ KVBars bars;
@@ -571,9 +605,9 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
 
     auto bar = [](uint64_t& b) { return smem_u32(&b); };
     const uint32_t sK = smem_u32(smem);
-    const uint32_t sV = sK + kTileBytes;
-    const uint32_t sStage = sK + 2 * kTileBytes;
-    const float* stage_f = reinterpret_cast<const float*>(smem + 2 * kTileBytes);   // float view of the stages
+    const uint32_t sV = sK + C::kTileBytes;
+    const uint32_t sStage = sK + 2 * C::kTileBytes;
+    const float* stage_f = reinterpret_cast<const float*>(smem + 2 * C::kTileBytes);   // float view of the stages
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
@@ -609,9 +643,9 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         }
         if (n_q > 0 && elect_one_sync()) {
             const int32_t row = static_cast<int32_t>(kv_tile_global * kTileElems);
-            mbar_arrive_expect_tx(bar(bars.kv_full), 2 * kTileBytes);
+            mbar_arrive_expect_tx(bar(bars.kv_full), 2 * C::kTileBytes);
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
+            for (int c = 0; c < C::kChunks; ++c) {
                 tma_load_2d(sK + c * kTileElems * 128, &p.tmK, bar(bars.kv_full), c * 64, row);
                 tma_load_2d(sV + c * kTileElems * 128, &p.tmV, bar(bars.kv_full), c * 64, row);
             }
@@ -629,16 +663,16 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
                 break;
             }
             if (elect_one_sync()) {
-                const uint32_t st = sStage + s * kKVStageBytes;
+                const uint32_t st = sStage + s * C::kKVStageBytes;
                 const int32_t row = static_cast<int32_t>(qtile * kTileElems);
-                mbar_arrive_expect_tx(bar(bars.full[s]), 2 * kTileBytes + 2 * kTileElems * 4);
+                mbar_arrive_expect_tx(bar(bars.full[s]), 2 * C::kTileBytes + 2 * kTileElems * 4);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
+                for (int c = 0; c < C::kChunks; ++c) {
                     tma_load_2d(st + c * kTileElems * 128, &p.tmQ, bar(bars.full[s]), c * 64, row);
-                    tma_load_2d(st + kTileBytes + c * kTileElems * 128, &p.tmDO, bar(bars.full[s]), c * 64, row);
+                    tma_load_2d(st + C::kTileBytes + c * kTileElems * 128, &p.tmDO, bar(bars.full[s]), c * 64, row);
                 }
-                bulk_load_g2s(st + 2 * kTileBytes, p.lse + qtile * kTileElems, kTileElems * 4, bar(bars.full[s]));
-                bulk_load_g2s(st + 2 * kTileBytes + kTileElems * 4, p.delta + qtile * kTileElems, kTileElems * 4,
+                bulk_load_g2s(st + 2 * C::kTileBytes, p.lse + qtile * kTileElems, kTileElems * 4, bar(bars.full[s]));
+                bulk_load_g2s(st + 2 * C::kTileBytes + kTileElems * 4, p.delta + qtile * kTileElems, kTileElems * 4,
                               bar(bars.full[s]));
             }
             __syncwarp();
@@ -656,7 +690,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         const uint32_t tDV = tmem + kColDV, tDK = tmem + kColDK, tST = tmem + kColST, tDPT = tmem + kColDPT;
         const uint64_t dKj = make_smem_desc(sK, 16, 8 * 128, kSwizzle128B);
         const uint64_t dVj = make_smem_desc(sV, 16, 8 * 128, kSwizzle128B);
-        auto stage_of = [&](int i) { return sStage + (i % kBStages) * kKVStageBytes; };
+        auto stage_of = [&](int i) { return sStage + (i % kBStages) * C::kKVStageBytes; };
         // S^T(i) = K_j Q_i^T (both operands from shared memory)
         auto issue_s = [&](int i) -> bool {
             const int s = i % kBStages;
@@ -666,7 +700,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             const uint64_t dQk = make_smem_desc(stage_of(i), 16, 8 * 128, kSwizzle128B);   // K-major
             if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < kQKSteps; ++kk) {
+                for (int kk = 0; kk < C::kQKSteps; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128)) >> 4);
                     mma_f16_ss(tST, dKj + off, dQk + off, kIdesc, kk > 0 ? 1u : 0u);
                 }
@@ -677,10 +711,10 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         };
         // dP^T(i) = V_j dO_i^T (step i's stage has landed: issue_s(i) waited for it)
         auto issue_dp = [&](int i) {
-            const uint64_t dDOk = make_smem_desc(stage_of(i) + kTileBytes, 16, 8 * 128, kSwizzle128B);
+            const uint64_t dDOk = make_smem_desc(stage_of(i) + C::kTileBytes, 16, 8 * 128, kSwizzle128B);
             if (elect_one_sync()) {
 #pragma unroll
-                for (int kk = 0; kk < kQKSteps; ++kk) {
+                for (int kk = 0; kk < C::kQKSteps; ++kk) {
                     const uint64_t off = static_cast<uint64_t>((((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128)) >> 4);
                     mma_f16_ss(tDPT, dVj + off, dDOk + off, kIdesc, kk > 0 ? 1u : 0u);
                 }
@@ -715,7 +749,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             tc_fence_after();
             const uint32_t st = stage_of(i);
             const uint64_t dQm = make_smem_desc(st, kTileElems * 128, 8 * 128, kSwizzle128B);   // MN-major
-            const uint64_t dDOm = make_smem_desc(st + kTileBytes, kTileElems * 128, 8 * 128, kSwizzle128B);
+            const uint64_t dDOm = make_smem_desc(st + C::kTileBytes, kTileElems * 128, 8 * 128, kSwizzle128B);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kDQSteps; ++kk) {
@@ -725,8 +759,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
                     const uint32_t a = (kk >> 1) * 32 + (kk & 1) * 8;
                     const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
                     const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-                    mma_f16_ts(tDV, tDPT + a, dDOm + off, kIdescMN, acc);
-                    mma_f16_ts(tDK, tDPT + a + 16, dQm + off, kIdescMN, acc);
+                    mma_f16_ts(tDV, tDPT + a, dDOm + off, C::kIdescMN, acc);
+                    mma_f16_ts(tDK, tDPT + a + 16, dQm + off, C::kIdescMN, acc);
                 }
                 mma_commit(bar(bars.empty[s]));
                 if (i == n_q - 1) mma_commit(bar(bars.final_));
@@ -804,7 +838,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
                 len[d] = qhi[d] - qlo[d] + 1;                      // <= 0: empty
                 full = full && len[d] > 0 && lo[d] <= 0 && lo[d] + len[d] >= p.tile[d];
             }
-            const float* lse_s = stage_f + s * (kKVStageBytes / 4) + 2 * (kTileBytes / 4);
+            const float* lse_s = stage_f + s * (C::kKVStageBytes / 4) + 2 * (C::kTileBytes / 4);
             const float* delta_s = lse_s + kTileElems;
             const float2 sc2 = make_float2(scale_log2, scale_log2);
             const float2 nlog2e = make_float2(-kBLog2e, -kBLog2e);
@@ -873,14 +907,14 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             tc_fence_after();
 #pragma unroll
             for (int which = 0; which < 2; ++which) {              // 0: dv, 1: dk (times scale)
-                uint8_t* dst_row = static_cast<uint8_t*>(which == 0 ? p.dv : p.dk) + grow * kRowBytes +
-                                   half * (kRowBytes / 2);
+                uint8_t* dst_row = static_cast<uint8_t*>(which == 0 ? p.dv : p.dk) + grow * C::kRowBytes +
+                                   half * (C::kRowBytes / 2);
                 const float mul = which == 0 ? 1.0f : p.scale;
 #pragma unroll
-                for (int pc = 0; pc < 2; ++pc) {
+                for (int pc = 0; pc < C::kHalfPieces; ++pc) {
                     uint32_t r[32];
                     if (n_q > 0) {
-                        tmem_ld32(tmem + (which == 0 ? kColDV : kColDK) + lane_addr + half * 64 + pc * 32, r);
+                        tmem_ld32(tmem + (which == 0 ? kColDV : kColDK) + lane_addr + half * (D / 2) + pc * 32, r);
                         tmem_wait_ld();
                         bwd_reg_fence(r);
                     } else {
@@ -914,19 +948,28 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
 
 // delta_i = <dout_i, out_i> (fp32 accumulation of the bf16 rows), one warp per
 // tiled row: 128 elements, 4 per lane.
+template <int D>
 __global__ void gna_bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, const __nv_bfloat16* __restrict__ dout,
                                      float* __restrict__ delta, int64_t rows)
 {
     const int64_t r = static_cast<int64_t>(blockIdx.x) * (blockDim.x / 32) + threadIdx.x / 32;
     if (r >= rows) return;
     const int lane = threadIdx.x % 32;
-    const uint2 o = *reinterpret_cast<const uint2*>(out + r * kD + lane * 4);
-    const uint2 g = *reinterpret_cast<const uint2*>(dout + r * kD + lane * 4);
-    const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.x));
-    const float2 o1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.y));
-    const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
-    const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
-    float acc = o0.x * g0.x + o0.y * g0.y + o1.x * g1.x + o1.y * g1.y;
+    float acc;
+    if constexpr (D == 128) {
+        const uint2 o = *reinterpret_cast<const uint2*>(out + r * D + lane * 4);
+        const uint2 g = *reinterpret_cast<const uint2*>(dout + r * D + lane * 4);
+        const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.x));
+        const float2 o1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&o.y));
+        const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
+        const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
+        acc = o0.x * g0.x + o0.y * g0.y + o1.x * g1.x + o1.y * g1.y;
+    } else {
+        static_assert(D == 64, "head_dim 64 or 128");
+        const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(out + r * D + lane * 2));
+        const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + r * D + lane * 2));
+        acc = o0.x * g0.x + o0.y * g0.y;
+    }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
     if (lane == 0) delta[r] = acc;
@@ -934,32 +977,64 @@ __global__ void gna_bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, cons
 
 }  // namespace
 
-cudaError_t launch_backward_dq(const BwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
+namespace {
+
+template <int D>
+cudaError_t launch_dq(const BwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
+{
+    using C = BwdCfg<D>;
+    static_assert(C::kSmemAlloc <= 232448 - 4096, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(gna_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    gna_bwd_dq_kernel<D><<<dim3(static_cast<unsigned>(num_q_tiles)), kBThreads, C::kSmemAlloc, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_dkdv(const BwdKVParams& p, int64_t num_kv_tiles, cudaStream_t stream)
+{
+    using C = BwdCfg<D>;
+    static_assert(C::kKVSmemAlloc <= 232448 - 4096, "shared memory budget");
+    cudaError_t e = cudaFuncSetAttribute(gna_bwd_dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kKVSmemAlloc);
+    if (e != cudaSuccess) return e;
+    gna_bwd_dkdv_kernel<D><<<dim3(static_cast<unsigned>(num_kv_tiles)), kBThreads, C::kKVSmemAlloc, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward_dq(const BwdParams& p, int head_dim, int64_t num_q_tiles, cudaStream_t stream)
 {
     if (num_q_tiles <= 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gna_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    gna_bwd_dq_kernel<<<dim3(static_cast<unsigned>(num_q_tiles)), kBThreads, kSmemAlloc, stream>>>(p);
-    return cudaGetLastError();
+    if (head_dim == 128) return launch_dq<128>(p, num_q_tiles, stream);
+    if (head_dim == 64) return launch_dq<64>(p, num_q_tiles, stream);
+    return cudaErrorNotSupported;
 }
 
-cudaError_t launch_backward_dkdv(const BwdKVParams& p, int64_t num_kv_tiles, cudaStream_t stream)
+cudaError_t launch_backward_dkdv(const BwdKVParams& p, int head_dim, int64_t num_kv_tiles, cudaStream_t stream)
 {
     if (num_kv_tiles <= 0) return cudaSuccess;
-    cudaError_t e =
-        cudaFuncSetAttribute(gna_bwd_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKVSmemAlloc);
-    if (e != cudaSuccess) return e;
-    gna_bwd_dkdv_kernel<<<dim3(static_cast<unsigned>(num_kv_tiles)), kBThreads, kKVSmemAlloc, stream>>>(p);
-    return cudaGetLastError();
+    if (head_dim == 128) return launch_dkdv<128>(p, num_kv_tiles, stream);
+    if (head_dim == 64) return launch_dkdv<64>(p, num_kv_tiles, stream);
+    return cudaErrorNotSupported;
 }
 
-cudaError_t launch_backward_delta(const void* out, const void* dout, float* delta, int64_t rows, cudaStream_t stream)
+cudaError_t launch_backward_delta(const void* out, const void* dout, float* delta, int64_t rows, int head_dim,
+                                  cudaStream_t stream)
 {
     if (rows <= 0) return cudaSuccess;
     const int warps = 8;
     const int64_t blocks = (rows + warps - 1) / warps;
-    gna_bwd_delta_kernel<<<dim3(static_cast<unsigned>(blocks)), warps * 32, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta, rows);
+    const auto* o = static_cast<const __nv_bfloat16*>(out);
+    const auto* g = static_cast<const __nv_bfloat16*>(dout);
+    if (head_dim == 128)
+        gna_bwd_delta_kernel<128><<<dim3(static_cast<unsigned>(blocks)), warps * 32, 0, stream>>>(o, g, delta, rows);
+    else if (head_dim == 64)
+        gna_bwd_delta_kernel<64><<<dim3(static_cast<unsigned>(blocks)), warps * 32, 0, stream>>>(o, g, delta, rows);
+    else
+        return cudaErrorNotSupported;
     return cudaGetLastError();
 }
 

@@ -64,17 +64,17 @@ cudaError_t launch_forward(const FwdParams& p, int head_dim, int elem_size, int6
 // Device status word: read-and-clear.
 cudaError_t read_and_clear_status(int* status, cudaStream_t stream);
 
-// Parameters of one dQ launch of the backward pass (bf16, head_dim 128; all
-// tensors tiled except kv, which is k in the value layout).
+// Parameters of one dQ launch of the backward pass (bf16, head_dim 64 or 128;
+// all tensors tiled except kv, which is k in the value layout).
 struct BwdParams {
-    CUtensorMap tmK;             // 2-D TMA view [rows, 128] of the tiled k
-    CUtensorMap tmV;             // 2-D TMA view [rows, 128] of the tiled v
-    CUtensorMap tmKv;            // 2-D TMA view [rows, 128] of k in the value layout
-    const void* q;               // tiled q [rows, 128]
-    const void* dout;            // tiled dout [rows, 128]
+    CUtensorMap tmK;             // 2-D TMA view [rows, head_dim] of the tiled k
+    CUtensorMap tmV;             // 2-D TMA view [rows, head_dim] of the tiled v
+    CUtensorMap tmKv;            // 2-D TMA view [tiles * head_dim, 128] of k in the value layout
+    const void* q;               // tiled q [rows, head_dim]
+    const void* dout;            // tiled dout [rows, head_dim]
     const float* lse;            // tiled lse [rows] of the forward (natural log)
     const float* delta;          // tiled <dout, out> [rows]
-    void* dq;                    // tiled bf16 dq [rows, 128]
+    void* dq;                    // tiled bf16 dq [rows, head_dim]
     int dims[3], win[3], str[3], off[3];
     int tile[3], tlog[3], nt[3];
     int tiles_per_head;
@@ -82,28 +82,29 @@ struct BwdParams {
     int fault_skip_kv;           // test hook: >= 0 makes the producer skip that KV load
 };
 
-// Parameters of one dK / dV launch of the backward pass (bf16, head_dim 128,
-// all tensors tiled).
+// Parameters of one dK / dV launch of the backward pass (bf16, head_dim 64 or
+// 128, all tensors tiled).
 struct BwdKVParams {
-    CUtensorMap tmQ;             // 2-D TMA views [rows, 128] of the tiled q, dout, k and v
+    CUtensorMap tmQ;             // 2-D TMA views [rows, head_dim] of the tiled q, dout, k and v
     CUtensorMap tmDO;
     CUtensorMap tmK;
     CUtensorMap tmV;
     const float* lse;            // tiled lse [rows] of the forward (natural log)
     const float* delta;          // tiled <dout, out> [rows]
-    void* dk;                    // tiled bf16 dk [rows, 128]
-    void* dv;                    // tiled bf16 dv [rows, 128]
+    void* dk;                    // tiled bf16 dk [rows, head_dim]
+    void* dv;                    // tiled bf16 dv [rows, head_dim]
     int dims[3], win[3], str[3], off[3];
     int tile[3], tlog[3], nt[3];
     int tiles_per_head;
     float scale;
 };
 
-cudaError_t launch_backward_dkdv(const BwdKVParams& p, int64_t num_kv_tiles, cudaStream_t stream);
-
-// dQ over num_q_tiles CTAs, and delta = <dout, out> over `rows` tiled rows.
-cudaError_t launch_backward_dq(const BwdParams& p, int64_t num_q_tiles, cudaStream_t stream);
-cudaError_t launch_backward_delta(const void* out, const void* dout, float* delta, int64_t rows,
+// dK / dV over num_kv_tiles CTAs, dQ over num_q_tiles CTAs, and delta =
+// <dout, out> over `rows` tiled rows; head_dim 64 or 128 (else
+// cudaErrorNotSupported).
+cudaError_t launch_backward_dkdv(const BwdKVParams& p, int head_dim, int64_t num_kv_tiles, cudaStream_t stream);
+cudaError_t launch_backward_dq(const BwdParams& p, int head_dim, int64_t num_q_tiles, cudaStream_t stream);
+cudaError_t launch_backward_delta(const void* out, const void* dout, float* delta, int64_t rows, int head_dim,
                                   cudaStream_t stream);
 // Status word of the backward kernels: read-and-clear.
 cudaError_t read_and_clear_bwd_status(int* status, cudaStream_t stream);

@@ -57,8 +57,7 @@ def gpu_backward(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEAD
     return [r.float().cpu().numpy() for r in res], (dq_t, dk_t, dv_t)
 
 
-def _check_grads(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
-    d = 128
+def _check_grads(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER, d=128):
     q, k, v, dout = (to_bf16(normal_raster(seed + i, B, dims, heads, d)) for i in range(4))
     got, _ = gpu_backward(q, k, v, dout, dims, window, stride, tile=tile, rule=rule)
     orule = oracle.LEADER_CENTER if rule == G.GNA_LEADER_CENTER else oracle.LEADER_LITERAL
@@ -70,7 +69,7 @@ def _check_grads(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEA
         info = f"{name}: max|err|={err.max():.3e} max|ref|={np.abs(r).max():.3e} relRMS={rel:.3e}"
         print(info)
         record_parity(kind="backward", grad=name, seed=seed, dims=list(dims), window=list(window),
-                      stride=list(stride), heads=heads, B=B, max_abs_err=float(err.max()),
+                      stride=list(stride), heads=heads, B=B, head_dim=d, max_abs_err=float(err.max()),
                       max_abs_ref=float(np.abs(r).max()), rel_rms=rel)
         assert np.isfinite(g).all(), info
         assert rel < REL_RMS_GRAD, info
@@ -90,9 +89,26 @@ def test_gradients_small_grids_all_elements(B, heads, dims, window, stride, tile
     _check_grads(8000 + sum(dims), B, heads, dims, window, stride, tile=tile, rule=rule)
 
 
+@pytest.mark.parametrize("B,heads,dims,window,stride,tile,rule", [
+    (1, 2, (4, 16, 20), (3, 7, 9), (1, 1, 1), None, G.GNA_LEADER_CENTER),
+    (2, 2, (5, 19, 23), (3, 9, 11), (1, 2, 3), None, G.GNA_LEADER_CENTER),     # ragged: every tile padded
+    (1, 2, (6, 20, 24), (4, 8, 8), (2, 4, 4), None, G.GNA_LEADER_LITERAL),
+    (1, 2, (3, 17, 40), (3, 7, 13), (1, 2, 5), (1, 8, 16), G.GNA_LEADER_CENTER),
+    (1, 3, (1, 45, 37), (1, 12, 9), (1, 1, 1), None, G.GNA_LEADER_CENTER),     # 2-D
+    (1, 2, (2, 8, 16), (2, 8, 16), (1, 1, 1), None, G.GNA_LEADER_CENTER),      # window = grid
+])
+def test_gradients_head_dim_64_small_grids_all_elements(B, heads, dims, window, stride, tile, rule):
+    """head_dim 64: one 128-byte span per token row, dQ / dK / dV accumulators of 64 columns."""
+    _check_grads(8300 + sum(dims), B, heads, dims, window, stride, tile=tile, rule=rule, d=64)
+
+
 def test_gradients_mid_size_video_grid():
     """Several KV tiles per dimension and full interior tiles (8x24x40 tokens, 4 heads)."""
     _check_grads(8100, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1))
+
+
+def test_gradients_head_dim_64_mid_size_video_grid():
+    _check_grads(8400, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1), d=64)
 
 
 def test_gradients_repeat_runs_bit_identical():

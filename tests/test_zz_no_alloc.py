@@ -46,9 +46,8 @@ def test_no_alloc_backward_rejects_sizes_beyond_its_workspace():
     assert st == G.GNA_ERR_INVALID_ARG and "NULL" in L.gna_last_error().decode()
 
 
-def _problem(seed, B, heads, dims, window, stride):
+def _problem(seed, B, heads, dims, window, stride, d):
     """Tiled bf16 inputs on the GPU and the forward's out and lse."""
-    d = 128
     dev = torch.device("cuda")
     shp = G.tiled_shape(B, heads, dims, d)
     x = {}
@@ -67,8 +66,7 @@ def _problem(seed, B, heads, dims, window, stride):
     return x
 
 
-def _regular_backward(x, B, heads, dims, window, stride):
-    d = 128
+def _regular_backward(x, B, heads, dims, window, stride, d):
     delta = torch.empty(x["lse"].shape, dtype=torch.float32, device=x["q"].device)
     dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
     G.gna_backward_delta(x["out"], x["dout"], delta, B, heads, dims, d)
@@ -79,23 +77,24 @@ def _regular_backward(x, B, heads, dims, window, stride):
     return dq, dk, dv
 
 
-def _no_alloc_backward(x, B, heads, dims, window, stride):
+def _no_alloc_backward(x, B, heads, dims, window, stride, d):
     dq, dk, dv = (torch.empty_like(x["q"]) for _ in range(3))
     G.gna_backward_noalloc(x["q"], x["k"], x["k_value"], x["v"], x["out"], x["dout"], x["lse"], dq, dk, dv, B,
-                           heads, dims, window, stride, 128)
+                           heads, dims, window, stride, d)
     return dq, dk, dv
 
 
 @pytest.mark.gpu
 def test_no_alloc_backward_matches_regular_entry_points_twice_in_a_row():
     problems = [
-        (9100, 2, 3, (6, 20, 24), (4, 9, 8), (2, 3, 8)),      # larger: fills more of the shared array
-        (9200, 1, 2, (3, 17, 19), (3, 7, 5), (1, 2, 1)),      # smaller, ragged: runs over the first's leftovers
+        (9100, 2, 3, (6, 20, 24), (4, 9, 8), (2, 3, 8), 128),   # larger: fills more of the shared array
+        (9200, 1, 2, (3, 17, 19), (3, 7, 5), (1, 2, 1), 128),   # smaller, ragged: runs over the first's leftovers
+        (9250, 1, 2, (5, 19, 23), (3, 9, 11), (1, 2, 3), 64),   # head_dim 64
     ]
-    for seed, B, heads, dims, window, stride in problems:
-        x = _problem(seed, B, heads, dims, window, stride)
-        got = _no_alloc_backward(x, B, heads, dims, window, stride)
-        want = _regular_backward(x, B, heads, dims, window, stride)
+    for seed, B, heads, dims, window, stride, d in problems:
+        x = _problem(seed, B, heads, dims, window, stride, d)
+        got = _no_alloc_backward(x, B, heads, dims, window, stride, d)
+        want = _regular_backward(x, B, heads, dims, window, stride, d)
         G.gna_get_status()
         torch.cuda.synchronize()
         for name, g, w in zip(("dq", "dk", "dv"), got, want):
