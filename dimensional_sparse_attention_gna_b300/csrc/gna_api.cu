@@ -817,6 +817,7 @@ gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, co
     if ((st = make_tile_map(&p.tmK, k, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_tile_map(&p.tmV, v, rows, head_dim, 2)) != GNA_OK) return st;
     if ((st = make_value_map(&p.tmKv, k_value, nq, head_dim, 2)) != GNA_OK) return st;
+    if ((st = make_tile_map(&p.tmDO, dout, rows, head_dim, 2)) != GNA_OK) return st;
     cudaError_t e = gna::launch_backward_dq(p, head_dim, nq, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "backward dq launch");
     t_last_error.clear();

@@ -14,19 +14,22 @@
 // of KV tiles exactly as the forward does (GNA page §1.1: the stride decides
 // which KV tiles a Q tile visits; §2.1: the element mask only on partial KV
 // tiles).  One CTA per 128-query tile, 320 threads:
-//   warp 0      TMA producer: per KV tile, K (tiled), V (tiled) and K in the
-//               value layout (feature-major) through a 2-stage ring
+//   warp 0      TMA producer: dO once; per KV tile K, V (tiled) and K in the
+//               value layout (feature-major), each through a 2-slot ring of
+//               its own, so a slot is refilled as soon as its one product is done
 //   warp 1      TMEM allocator and tcgen05.mma issuer
 //   warps 2..9  dS: thread = (query row, half of the 128 key columns)
-// TMEM (512 columns): dQ [0, 128), S [128, 256), dP [256, 384), Q [384, 448),
-// dO [448, 512).  Per KV tile: S = Q K^T and dP = dO V^T (A from TMEM), then
-// dQ += dS K with dS (bf16) in TMEM as the A operand: each half writes its 32
-// columns of dS over the front of its own 64 dP columns, so the halves never
-// touch each other's values, and the S columns are free as soon as the dS
-// warps hold S in registers: S of the next KV tile is computed while they
-// work.  The element mask of a partial tile is one 32-bit word per 32 key
-// columns (box_mask_word).  K in the value layout is the K-major B operand of
-// dS K, as V is for P V in the forward.
+// TMEM (512 columns): dQ [0, 128), S [128, 256), dP [256, 384), dS [384, 448),
+// Q [448, 512).  Per KV tile: S = Q K^T (A from TMEM), dP = dO V^T (both
+// operands from shared memory), then dQ += dS K with dS (bf16) in TMEM as the
+// A operand and K in the value layout as the K-major B operand (as V is for
+// P V in the forward).  S, dP and dS each have columns of their own: the dS
+// warps hand S and dP back as soon as they hold them in registers, so S and
+// dP of the next KV tile are computed while they form dS, and only the store
+// of dS waits for the previous dQ product.  No TMEM reuse depends on the
+// order in which the tensor core executes products: every reuse waits on a
+// barrier.  The element mask of a partial tile is one 32-bit word per 32 key
+// columns (box_mask_word).
 //
 // Every mbarrier wait is bounded; a role that gives up raises the abort flag
 // and the device status word, and the CTA drains and exits.
@@ -50,8 +53,8 @@ constexpr uint32_t kBTmemCols = 512;
 constexpr uint32_t kColDQ = 0;
 constexpr uint32_t kColS = 128;
 constexpr uint32_t kColDP = 256;
-constexpr uint32_t kColQ = 384;
-constexpr uint32_t kColDO = 448;
+constexpr uint32_t kColDS = 384;
+constexpr uint32_t kColQ = 448;
 constexpr int kBStages = 2;
 constexpr float kBLog2e = 1.4426950408889634f;
 
@@ -64,13 +67,12 @@ template <int D>
 struct BwdCfg {
     static constexpr int kRowBytes = D * 2;                    // bytes per token row
     static constexpr int kChunks = kRowBytes / 128;            // 128-byte spans per row (TMA boxes per tile)
-    static constexpr int kTileBytes = kTileElems * kRowBytes;  // one 128-token tile
-    static constexpr int kStageBytes = 3 * kTileBytes;         // K, V, K (value layout)
+    static constexpr int kTileBytes = kTileElems * kRowBytes;  // one 128-token tile (either layout)
     // at least ~116 KB, so that one CTA (which takes all 512 TMEM columns) is
     // resident per SM and a second one never waits in the TMEM allocation
     static constexpr int kMinSmem = 118784;
-    static constexpr int kSmemAlloc = (kStageBytes * kBStages + 1024) > kMinSmem ? (kStageBytes * kBStages + 1024)
-                                                                                 : kMinSmem;
+    // dQ kernel: dO, then two slots each of K, V and K (value layout)
+    static constexpr int kDQSmemAlloc = (7 * kTileBytes + 1024) > kMinSmem ? (7 * kTileBytes + 1024) : kMinSmem;
     static constexpr int kQKSteps = kRowBytes / 32;            // MMA k-steps over the head dimension
     static constexpr int kHalfWords = kRowBytes / 8;           // TMEM columns of half a Q / dO row
     static constexpr int kHalfPieces = D / 64;                 // 32-column pieces of half a dQ / dK / dV row
@@ -82,14 +84,20 @@ struct BwdCfg {
     static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
+// the dQ kernel's three shared-memory rings (one per operand of a KV tile)
+enum { kRingK = 0, kRingV = 1, kRingKv = 2, kRings = 3 };
+
 struct BwdBars {
-    uint64_t qdo_full;            // Q and dO rows stored in TMEM (8 warps)
-    uint64_t full[kBStages];      // K, V, K (value layout) of a KV tile landed
-    uint64_t empty[kBStages];     // the KV tile's three MMAs are done
+    uint64_t q_full;              // Q rows stored in TMEM (8 warps)
+    uint64_t do_full;             // the dO tile landed in shared memory
+    uint64_t full[kRings][2];     // K / V / K (value layout) of a KV tile landed in its slot
+    uint64_t empty[kRings][2];    // the one product that reads the slot is done
     uint64_t s_full;              // S of KV tile j is in TMEM (one phase per tile)
     uint64_t s_free;              // the dS warps hold S(j) in registers: S may take S(j + 1) (8 warps)
     uint64_t dp_full;             // dP of KV tile j is in TMEM
-    uint64_t ds_full;             // dS of KV tile j is in TMEM, over the front of dP (8 warps)
+    uint64_t dp_free;             // the dS warps hold dP(j) in registers (8 warps)
+    uint64_t ds_full;             // dS of KV tile j is in TMEM (8 warps)
+    uint64_t ds_free;             // dQ(j) is done: dS may take dS(j + 1)
     uint64_t dq_final;            // the last dQ product is done
     uint64_t drain;
 };
@@ -211,19 +219,28 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
     const int64_t kv_tile_base = bh * p.tiles_per_head;       // first tile of this (b, head) plane
 
     auto bar = [](uint64_t& b) { return smem_u32(&b); };
-    const uint32_t s_base = smem_u32(smem);
+    // shared memory: dO, then slots K0 K1 V0 V1 Kv0 Kv1 (one tile each)
+    const uint32_t sDO = smem_u32(smem);
+    auto slot_addr = [&](int ring, int slot) {
+        return sDO + static_cast<uint32_t>((1 + 2 * ring + slot) * C::kTileBytes);
+    };
 
     if (threadIdx.x == 0) {
         abort_flag = 0;
-        mbar_init(bar(bars.qdo_full), kBSoftmaxWarps);
-        for (int s = 0; s < kBStages; ++s) {
-            mbar_init(bar(bars.full[s]), 1);
-            mbar_init(bar(bars.empty[s]), 1);
+        mbar_init(bar(bars.q_full), kBSoftmaxWarps);
+        mbar_init(bar(bars.do_full), 1);
+        for (int r = 0; r < kRings; ++r) {
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(bar(bars.full[r][s]), 1);
+                mbar_init(bar(bars.empty[r][s]), 1);
+            }
         }
         mbar_init(bar(bars.s_full), 1);
         mbar_init(bar(bars.s_free), kBSoftmaxWarps);
         mbar_init(bar(bars.dp_full), 1);
+        mbar_init(bar(bars.dp_free), kBSoftmaxWarps);
         mbar_init(bar(bars.ds_full), kBSoftmaxWarps);
+        mbar_init(bar(bars.ds_free), 1);
         mbar_init(bar(bars.dq_final), 1);
         mbar_init(bar(bars.drain), 1);
         fence_mbarrier_init();
@@ -240,61 +257,76 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
     if (warp == 0) {
         // ============================================================ TMA producer
         if (elect_one_sync()) {
+            prefetch_tensormap(&p.tmDO);
             prefetch_tensormap(&p.tmK);
             prefetch_tensormap(&p.tmV);
             prefetch_tensormap(&p.tmKv);
+            // this Q tile's dO rows: 128 rows x 64 elements per box (128-byte swizzle)
+            mbar_arrive_expect_tx(bar(bars.do_full), C::kTileBytes);
+            const int32_t row = static_cast<int32_t>(q_tile_global * kTileElems);
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_2d(sDO + c * kTileElems * 128, &p.tmDO, bar(bars.do_full), c * 64, row);
         }
-        int issued = 0;
+        __syncwarp();
+        int issued[kRings] = {0, 0, 0};
         bool early = false;
         int kc[3] = {box.k0[0], box.k0[1], box.k0[2]};
-        for (int j = 0; j < n_kv; ++j, bwd_odometer(kc, box)) {
-            const int s = j % kBStages;
-            const int64_t tile = kv_tile_base + (kc[0] * p.nt[1] + kc[1]) * p.nt[2] + kc[2];
-            if (j >= kBStages &&
-                !__all_sync(0xffffffffu, mbar_wait(bar(bars.empty[s]), ((j / kBStages) & 1) ^ 1, &abort_flag, &g_bwd_status))) {
-                early = true;
-                break;
-            }
+        for (int j = 0; j < n_kv && !early; ++j, bwd_odometer(kc, box)) {
             if (j == p.fault_skip_kv) { early = true; break; }   // test hook: consumers wait in vain
-            if (elect_one_sync()) {
-                const uint32_t st = s_base + s * C::kStageBytes;
-                mbar_arrive_expect_tx(bar(bars.full[s]), C::kStageBytes);
-                const int32_t row = static_cast<int32_t>(tile * kTileElems);
-                const int32_t vrow = static_cast<int32_t>(tile * D);
-#pragma unroll
-                for (int c = 0; c < C::kChunks; ++c) {
-                    // K and V tiles: 128 rows x 64 elements per box (128-byte swizzle)
-                    tma_load_2d(st + c * kTileElems * 128, &p.tmK, bar(bars.full[s]), c * 64, row);
-                    tma_load_2d(st + C::kTileBytes + c * kTileElems * 128, &p.tmV, bar(bars.full[s]), c * 64, row);
+            const int slot = j & 1;
+            const int64_t tile = kv_tile_base + (kc[0] * p.nt[1] + kc[1]) * p.nt[2] + kc[2];
+            for (int r = 0; r < kRings; ++r) {
+                // the slot's previous tile (j - 2) is done with it
+                if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(bars.empty[r][slot]), ((j >> 1) & 1) ^ 1,
+                                                                 &abort_flag, &g_bwd_status))) {
+                    early = true;
+                    break;
                 }
+                if (elect_one_sync()) {
+                    const uint32_t dst = slot_addr(r, slot);
+                    const uint32_t fb = bar(bars.full[r][slot]);
+                    mbar_arrive_expect_tx(fb, C::kTileBytes);
+                    if (r == kRingKv) {
+                        // K in the value layout: D rows x 64 tokens per box
+                        const int32_t vrow = static_cast<int32_t>(tile * D);
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    // K in the value layout: d rows x 64 tokens per box
-                    tma_load_2d(st + 2 * C::kTileBytes + c * D * 128, &p.tmKv, bar(bars.full[s]), c * 64, vrow);
+                        for (int c = 0; c < 2; ++c) tma_load_2d(dst + c * D * 128, &p.tmKv, fb, c * 64, vrow);
+                    } else {
+                        // K or V tile: 128 rows x 64 elements per box
+                        const int32_t row = static_cast<int32_t>(tile * kTileElems);
+#pragma unroll
+                        for (int c = 0; c < C::kChunks; ++c)
+                            tma_load_2d(dst + c * kTileElems * 128, r == kRingK ? &p.tmK : &p.tmV, fb, c * 64, row);
+                    }
                 }
+                __syncwarp();
+                ++issued[r];
             }
-            __syncwarp();
-            ++issued;
         }
-        if (early) {
-            // a skipped load (test hook) is left for the consumers' waits to find
-            if (p.fault_skip_kv < 0 && lane == 0) bwd_raise(&abort_flag);
-            const volatile int never = 0;
-            for (int j = (issued > kBStages ? issued - kBStages : 0); j < issued; ++j)
-                mbar_wait(bar(bars.full[j % kBStages]), (j / kBStages) & 1, &never);
-        }
+        // a skipped load (test hook) is left for the consumers' waits to find
+        if (early && p.fault_skip_kv < 0 && lane == 0) bwd_raise(&abort_flag);
+        // every load this warp issued lands before the CTA may exit (the last
+        // load of each slot is the slot's latest phase)
+        const volatile int never = 0;
+        for (int r = 0; r < kRings; ++r)
+            for (int j = (issued[r] > 2 ? issued[r] - 2 : 0); j < issued[r]; ++j)
+                mbar_wait(bar(bars.full[r][j & 1]), (j >> 1) & 1, &never);
+        mbar_wait(bar(bars.do_full), 0, &never);
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         const uint32_t tDQ = tmem + kColDQ, tS = tmem + kColS, tDP = tmem + kColDP;
-        const uint32_t tQ = tmem + kColQ, tDO = tmem + kColDO;
-        const uint64_t d0 = make_smem_desc(s_base, 16, 8 * 128, kSwizzle128B);
-        // S(j) = Q K(j)^T and dP(j) = dO V(j)^T, from TMEM A operands
+        const uint32_t tDS = tmem + kColDS, tQ = tmem + kColQ;
+        const uint64_t dDO = make_smem_desc(sDO, 16, 8 * 128, kSwizzle128B);
+        auto wait_slot = [&](int r, int j) -> bool {
+            return __all_sync(0xffffffffu, mbar_wait(bar(bars.full[r][j & 1]), (j >> 1) & 1, &abort_flag,
+                                                     &g_bwd_status));
+        };
+        // S(j) = Q K(j)^T: A (Q) from TMEM
         auto issue_s = [&](int j) -> bool {
-            const int s = j % kBStages;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (j / kBStages) & 1, &abort_flag, &g_bwd_status)))
-                return false;
+            if (!wait_slot(kRingK, j)) return false;
             tc_fence_after();
-            const uint64_t dK = d0 + static_cast<uint64_t>((s * C::kStageBytes) >> 4);
+            const uint64_t dK = make_smem_desc(slot_addr(kRingK, j & 1), 16, 8 * 128, kSwizzle128B);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
@@ -303,63 +335,66 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
                     mma_f16_ts(tS, tQ + kk * 8, dK + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(bars.s_full));
+                mma_commit(bar(bars.empty[kRingK][j & 1]));
             }
             __syncwarp();
             return true;
         };
-        auto issue_dp = [&](int j) {       // K/V of tile j landed (issue_s(j) waited for them)
-            const int s = j % kBStages;
-            const uint64_t dV = d0 + static_cast<uint64_t>((s * C::kStageBytes + C::kTileBytes) >> 4);
+        // dP(j) = dO V(j)^T: both operands from shared memory
+        auto issue_dp = [&](int j) -> bool {
+            if (!wait_slot(kRingV, j)) return false;
+            tc_fence_after();
+            const uint64_t dV = make_smem_desc(slot_addr(kRingV, j & 1), 16, 8 * 128, kSwizzle128B);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
                     const int off = ((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128);
-                    mma_f16_ts(tDP, tDO + kk * 8, dV + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
+                    mma_f16_ss(tDP, dDO + static_cast<uint64_t>(off >> 4), dV + static_cast<uint64_t>(off >> 4),
+                               kIdesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(bars.dp_full));
+                mma_commit(bar(bars.empty[kRingV][j & 1]));
             }
             __syncwarp();
+            return true;
         };
-        // Issue order  S(0) dP(0) | S(1) dQ(0) dP(1) | S(2) dQ(1) dP(2) | ...:
-        // S(j + 1) runs while the dS warps work on tile j (they release the S
-        // columns as soon as S(j) is in their registers), and dS(j) goes over
-        // the front of dP(j)'s columns, which dP(j + 1) overwrites after dQ(j)
-        // has read them: the tensor core executes one thread's MMAs in issue
-        // order.
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.qdo_full), 0, &abort_flag, &g_bwd_status));
-        if (ok && n_kv > 0) {
-            ok = issue_s(0);
-            if (ok) issue_dp(0);
-        }
-        for (int j = 0; ok && j < n_kv; ++j) {
-            const int s = j % kBStages;
-            if (j + 1 < n_kv) {
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.s_free), j & 1, &abort_flag, &g_bwd_status)) ||
-                    !issue_s(j + 1)) {
-                    ok = false;
-                    break;
-                }
-            }
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.ds_full), j & 1, &abort_flag, &g_bwd_status))) {
-                ok = false;
-                break;
-            }
+        // dQ += dS(j) K(j): A (dS) from TMEM, B = K in the value layout (K-major)
+        auto issue_dq = [&](int j) -> bool {
+            if (!wait_slot(kRingKv, j) ||
+                !__all_sync(0xffffffffu, mbar_wait(bar(bars.ds_full), j & 1, &abort_flag, &g_bwd_status)))
+                return false;
             tc_fence_after();
-            const uint64_t dKv = d0 + static_cast<uint64_t>((s * C::kStageBytes + 2 * C::kTileBytes) >> 4);
+            const uint64_t dKv = make_smem_desc(slot_addr(kRingKv, j & 1), 16, 8 * 128, kSwizzle128B);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kDQSteps; ++kk) {
-                    // k-step kk: key columns [16 kk, 16 kk + 16); dS of key column
-                    // half h sits at the front of dP columns [64 h, 64 h + 64)
-                    const uint32_t a = tDP + (kk >> 2) * 64 + (kk & 3) * 8;
+                    // k-step kk: key columns [16 kk, 16 kk + 16) = dS columns [8 kk, 8 kk + 8)
                     const int off = ((kk * 32) / 128) * (D * 128) + ((kk * 32) % 128);
-                    mma_f16_ts(tDQ, a, dKv + static_cast<uint64_t>(off >> 4), C::kIdescDQ, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_f16_ts(tDQ, tDS + kk * 8, dKv + static_cast<uint64_t>(off >> 4), C::kIdescDQ,
+                               (j > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar(bars.empty[s]));
+                mma_commit(bar(bars.empty[kRingKv][j & 1]));
+                mma_commit(bar(bars.ds_free));
                 if (j == n_kv - 1) mma_commit(bar(bars.dq_final));
             }
             __syncwarp();
-            if (j + 1 < n_kv) issue_dp(j + 1);
+            return true;
+        };
+        // Issue order  S(0) dP(0) | S(1) dP(1) dQ(0) | S(2) dP(2) dQ(1) | ...:
+        // S(j + 1) and dP(j + 1) wait only until the dS warps hold S(j) and
+        // dP(j) in registers, so they run while dS(j) is formed and stored.
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.q_full), 0, &abort_flag, &g_bwd_status)) &&
+                  __all_sync(0xffffffffu, mbar_wait(bar(bars.do_full), 0, &abort_flag, &g_bwd_status));
+        if (ok && n_kv > 0) ok = issue_s(0) && issue_dp(0);
+        for (int j = 0; ok && j < n_kv; ++j) {
+            if (j + 1 < n_kv) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.s_free), j & 1, &abort_flag, &g_bwd_status)) &&
+                     issue_s(j + 1) &&
+                     __all_sync(0xffffffffu, mbar_wait(bar(bars.dp_free), j & 1, &abort_flag, &g_bwd_status)) &&
+                     issue_dp(j + 1);
+                if (!ok) break;
+            }
+            ok = issue_dq(j);
         }
         if (!ok) {
             if (elect_one_sync()) {
@@ -391,13 +426,11 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
 #pragma unroll
         for (int d = 0; d < 3; ++d) st[d] = window_start(qpos[d], p.dims[d], p.win[d], p.str[d], p.off[d]);
 
-        // this half of the Q and dO rows -> TMEM (A operands of S and dP)
+        // this half of the Q row -> TMEM (the A operand of S)
         {
             constexpr int W = C::kHalfWords;
             const uint4* qs = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.q) + grow * C::kRowBytes +
                                                              half * (C::kRowBytes / 2));
-            const uint4* ds = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.dout) +
-                                                             grow * C::kRowBytes + half * (C::kRowBytes / 2));
             uint32_t w[W];
 #pragma unroll
             for (int i = 0; i < W / 4; ++i) {
@@ -405,16 +438,10 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
                 w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
             }
             bwd_tmem_st<W>(tmem + kColQ + lane_addr + half * W, w);
-#pragma unroll
-            for (int i = 0; i < W / 4; ++i) {
-                const uint4 v = __ldg(ds + i);
-                w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-            }
-            bwd_tmem_st<W>(tmem + kColDO + lane_addr + half * W, w);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bars.qdo_full));
+            if (lane == 0) mbar_arrive(bar(bars.q_full));
         }
         // lse (natural log) and delta of this query; padding rows contribute nothing
         const float lse2 = row_valid ? p.lse[grow] * kBLog2e : 0.0f;
@@ -434,11 +461,6 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             uint32_t rs[64];
             tmem_ld32(tmem + kColS + lane_addr + half * 64, *reinterpret_cast<uint32_t(*)[32]>(rs));
             tmem_ld32(tmem + kColS + lane_addr + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(rs + 32));
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(bars.s_free));
-            bwd_reg_fence(rs);
             bool full = true;
 #pragma unroll
             for (int d = 0; d < 3; ++d) full = full && kc[d] >= box.full_lo[d] && kc[d] <= box.full_hi[d];
@@ -446,46 +468,76 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             const int lo_t = st[0] - kc[0] * p.tile[0];
             const int lo_y = st[1] - kc[1] * p.tile[1];
             const int lo_x = st[2] - kc[2] * p.tile[2];
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars.s_free));
+            bwd_reg_fence(rs);
+            // p = exp2(s scale log2(e) - lse log2(e)), 0 outside the window, as
+            // bf16 pairs, while dP(j) is being computed.  Key column c of a
+            // 32-column piece is inside the window iff bit c of the piece's mask
+            // word is set (all set on a tile that lies in every window of the Q tile).
+            const float2 sc2 = make_float2(scale_log2, scale_log2);
+            const float2 nl2 = make_float2(-lse2, -lse2);
+            uint32_t pp[32];
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+                const uint32_t m = !row_valid ? 0u
+                                   : full     ? 0xffffffffu
+                                              : box_mask_word(half * 2 + pc, p.tlog[0], p.tlog[1], p.tlog[2], lo_t,
+                                                              lo_y, lo_x, p.win[0], p.win[1], p.win[2]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int c = 2 * i;
+                    const float s0 = (m >> c) & 1u ? __uint_as_float(rs[pc * 32 + c]) : -INFINITY;
+                    const float s1 = (m >> (c + 1)) & 1u ? __uint_as_float(rs[pc * 32 + c + 1]) : -INFINITY;
+                    const float2 x = bwd_ffma2(make_float2(s0, s1), sc2, nl2);
+                    __nv_bfloat162 h = __floats2bfloat162_rn(bwd_exp2(x.x), bwd_exp2(x.y));
+                    pp[pc * 16 + i] = *reinterpret_cast<uint32_t*>(&h);
+                }
+            }
             ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.dp_full), j & 1, &abort_flag, &g_bwd_status));
             if (!ok) {
                 bwd_raise(&abort_flag);
                 break;
             }
             tc_fence_after();
-            // two pieces of 32 key columns: S, dP -> dS (bf16) over the front of this half's dP columns
+            // this half row of dP(j) (both pieces in flight together); then its
+            // columns go back to the MMA warp for dP(j + 1)
+            uint32_t rp[64];
+            tmem_ld32(tmem + kColDP + lane_addr + half * 64, *reinterpret_cast<uint32_t(*)[32]>(rp));
+            tmem_ld32(tmem + kColDP + lane_addr + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(rp + 32));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(bars.dp_free));
+            bwd_reg_fence(rp);
+            // dS goes to its own columns once dQ(j - 1) has read dS(j - 1)
+            if (j > 0) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.ds_free), (j - 1) & 1, &abort_flag, &g_bwd_status));
+                if (!ok) {
+                    bwd_raise(&abort_flag);
+                    break;
+                }
+                tc_fence_after();
+            }
+            // dS = p (dP - delta) (bf16), two pieces of 32 key columns (16 TMEM columns each)
+            const float2 nd2 = make_float2(-delta, -delta);
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc) {
-                uint32_t rp[32];
-                const uint32_t col = half * 64 + pc * 32;
-                tmem_ld32(tmem + kColDP + lane_addr + col, rp);
-                // key column c of the piece is inside the window iff bit c is set
-                // (all set on a tile that lies in every window of the Q tile)
-                const uint32_t m = !row_valid ? 0u
-                                   : full     ? 0xffffffffu
-                                              : box_mask_word(static_cast<int>(col) >> 5, p.tlog[0], p.tlog[1],
-                                                              p.tlog[2], lo_t, lo_y, lo_x, p.win[0], p.win[1], p.win[2]);
-                tmem_wait_ld();
-                bwd_reg_fence(rp);
-                const float2 sc2 = make_float2(scale_log2, scale_log2);
-                const float2 nl2 = make_float2(-lse2, -lse2);
-                const float2 nd2 = make_float2(-delta, -delta);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int c = 2 * i;
-                    // p = exp2(s scale log2(e) - lse log2(e)), 0 outside the window
-                    const float s0 = (m >> c) & 1u ? __uint_as_float(rs[pc * 32 + c]) : -INFINITY;
-                    const float s1 = (m >> (c + 1)) & 1u ? __uint_as_float(rs[pc * 32 + c + 1]) : -INFINITY;
-                    const float2 x = bwd_ffma2(make_float2(s0, s1), sc2, nl2);
-                    const float2 pr = make_float2(bwd_exp2(x.x), bwd_exp2(x.y));
-                    // dS = p (dP - delta)
-                    const float2 dd = bwd_fadd2(make_float2(__uint_as_float(rp[c]), __uint_as_float(rp[c + 1])), nd2);
+                    const uint32_t hp = pp[pc * 16 + i];
+                    const float2 pr = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hp));
+                    const float2 dd = bwd_fadd2(make_float2(__uint_as_float(rp[pc * 32 + c]),
+                                                            __uint_as_float(rp[pc * 32 + c + 1])), nd2);
                     const float2 ds2 = bwd_fmul2(pr, dd);
                     __nv_bfloat162 h = __floats2bfloat162_rn(ds2.x, ds2.y);
                     pk[i] = *reinterpret_cast<uint32_t*>(&h);
                 }
-                // dS of these 32 keys over dP columns this thread already read
-                tmem_st16(tmem + kColDP + lane_addr + half * 64 + pc * 16, pk);
+                tmem_st16(tmem + kColDS + lane_addr + half * 32 + pc * 16, pk);
             }
             tmem_wait_st();
             tc_fence_before();
@@ -842,54 +894,69 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             const float* delta_s = lse_s + kTileElems;
             const float2 sc2 = make_float2(scale_log2, scale_log2);
             const float2 nlog2e = make_float2(-kBLog2e, -kBLog2e);
+            // P^T of this half row (bf16 pairs) while dP^T(i) is being computed:
+            // p = exp2(s scale log2(e) - lse log2(e)), 0 where the query does not
+            // reach the key (selected after the exponential: a padding query's
+            // lse is -inf, so its exponent may be anything there)
+            uint32_t pkp[32];
+#pragma unroll
+            for (int pc = 0; pc < 2; ++pc) {
+                // query column c of the piece reaches this key iff bit c is set
+                const uint32_t m = full ? 0xffffffffu
+                                        : box_mask_word(half * 2 + pc, p.tlog[0], p.tlog[1], p.tlog[2], lo[0], lo[1],
+                                                        lo[2], len[0], len[1], len[2]);
+                const int col0 = half * 64 + pc * 32;
+#pragma unroll
+                for (int g4 = 0; g4 < 8; ++g4) {
+                    const float4 L4 = *reinterpret_cast<const float4*>(lse_s + col0 + 4 * g4);
+#pragma unroll
+                    for (int e = 0; e < 4; e += 2) {
+                        const int k = 4 * g4 + e;                      // column of the piece
+                        const float2 lse2 = e == 0 ? make_float2(L4.x, L4.y) : make_float2(L4.z, L4.w);
+                        const float2 x = bwd_ffma2(make_float2(__uint_as_float(rs[pc * 32 + k]),
+                                                               __uint_as_float(rs[pc * 32 + k + 1])),
+                                                   sc2, bwd_fmul2(lse2, nlog2e));
+                        const float2 pr = make_float2((m >> k) & 1u ? bwd_exp2(x.x) : 0.0f,
+                                                      (m >> (k + 1)) & 1u ? bwd_exp2(x.y) : 0.0f);
+                        __nv_bfloat162 hp = __floats2bfloat162_rn(pr.x, pr.y);
+                        pkp[pc * 16 + k / 2] = *reinterpret_cast<uint32_t*>(&hp);
+                    }
+                }
+            }
             ok = __all_sync(0xffffffffu, mbar_wait(bar(bars.dp_full), i & 1, &abort_flag, &g_bwd_status));
             if (!ok) {
                 bwd_raise(&abort_flag);
                 break;
             }
             tc_fence_after();
-            // two pieces of 32 query columns; P^T and dS^T of a piece (16 columns
-            // each) go over the piece's own dP^T columns, which are read first
+            // dP^T(i) in two pieces of 32 query columns; P^T and dS^T of a piece
+            // (16 columns each) go over the piece's own dP^T columns once read.
+            // dS = p (dP - delta) with p as the bf16 value that dV's product reads.
 #pragma unroll
             for (int pc = 0; pc < 2; ++pc) {
                 const int col0 = half * 64 + pc * 32;
-                const uint32_t* rsp = rs + pc * 32;
                 uint32_t rp[32];
                 tmem_ld32(tmem + kColDPT + lane_addr + col0, rp);
-                // query column c of the piece reaches this key iff bit c is set
-                const uint32_t m = full ? 0xffffffffu
-                                        : box_mask_word(col0 >> 5, p.tlog[0], p.tlog[1], p.tlog[2], lo[0], lo[1], lo[2],
-                                                        len[0], len[1], len[2]);
                 tmem_wait_ld();
                 bwd_reg_fence(rp);
-                uint32_t pkp[16], pkd[16];
+                uint32_t pkd[16];
 #pragma unroll
                 for (int g4 = 0; g4 < 8; ++g4) {
-                    const float4 L4 = *reinterpret_cast<const float4*>(lse_s + col0 + 4 * g4);
                     const float4 D4 = *reinterpret_cast<const float4*>(delta_s + col0 + 4 * g4);
 #pragma unroll
                     for (int e = 0; e < 4; e += 2) {
-                        const int k = 4 * g4 + e;                      // column of the piece
-                        // p = exp2(s scale log2(e) - lse log2(e)), 0 where the query does not
-                        // reach the key (selected after the exponential: a padding query's
-                        // lse is -inf, so its exponent may be anything there)
-                        const float2 lse2 = e == 0 ? make_float2(L4.x, L4.y) : make_float2(L4.z, L4.w);
+                        const int k = 4 * g4 + e;
                         const float2 dl2 = e == 0 ? make_float2(D4.x, D4.y) : make_float2(D4.z, D4.w);
-                        const float2 x = bwd_ffma2(make_float2(__uint_as_float(rsp[k]), __uint_as_float(rsp[k + 1])), sc2,
-                                                   bwd_fmul2(lse2, nlog2e));
-                        const float2 pr = make_float2((m >> k) & 1u ? bwd_exp2(x.x) : 0.0f,
-                                                      (m >> (k + 1)) & 1u ? bwd_exp2(x.y) : 0.0f);
-                        // dS = p (dP - delta)
+                        const uint32_t hp = pkp[pc * 16 + k / 2];
+                        const float2 pr = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hp));
                         const float2 dd = bwd_fadd2(make_float2(__uint_as_float(rp[k]), __uint_as_float(rp[k + 1])),
                                                     make_float2(-dl2.x, -dl2.y));
                         const float2 ds2 = bwd_fmul2(pr, dd);
-                        __nv_bfloat162 hp = __floats2bfloat162_rn(pr.x, pr.y);
                         __nv_bfloat162 hd = __floats2bfloat162_rn(ds2.x, ds2.y);
-                        pkp[k / 2] = *reinterpret_cast<uint32_t*>(&hp);
                         pkd[k / 2] = *reinterpret_cast<uint32_t*>(&hd);
                     }
                 }
-                tmem_st16(tmem + kColDPT + lane_addr + col0, pkp);
+                tmem_st16(tmem + kColDPT + lane_addr + col0, *reinterpret_cast<const uint32_t(*)[16]>(pkp + pc * 16));
                 tmem_st16(tmem + kColDPT + lane_addr + col0 + 16, pkd);
             }
             tmem_wait_st();
@@ -983,11 +1050,12 @@ template <int D>
 cudaError_t launch_dq(const BwdParams& p, int64_t num_q_tiles, cudaStream_t stream)
 {
     using C = BwdCfg<D>;
-    static_assert(C::kSmemAlloc <= 232448 - 4096, "shared memory budget");
+    // the opt-in limit of 227 KB per block holds dynamic and static shared memory
+    static_assert(C::kDQSmemAlloc <= 232448 - 1024, "shared memory budget");
     cudaError_t e = cudaFuncSetAttribute(gna_bwd_dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemAlloc);
+                                         C::kDQSmemAlloc);
     if (e != cudaSuccess) return e;
-    gna_bwd_dq_kernel<D><<<dim3(static_cast<unsigned>(num_q_tiles)), kBThreads, C::kSmemAlloc, stream>>>(p);
+    gna_bwd_dq_kernel<D><<<dim3(static_cast<unsigned>(num_q_tiles)), kBThreads, C::kDQSmemAlloc, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -70,6 +70,7 @@ struct BwdParams {
     CUtensorMap tmK;             // 2-D TMA view [rows, head_dim] of the tiled k
     CUtensorMap tmV;             // 2-D TMA view [rows, head_dim] of the tiled v
     CUtensorMap tmKv;            // 2-D TMA view [tiles * head_dim, 128] of k in the value layout
+    CUtensorMap tmDO;            // 2-D TMA view [rows, head_dim] of the tiled dout
     const void* q;               // tiled q [rows, head_dim]
     const void* dout;            // tiled dout [rows, head_dim]
     const float* lse;            // tiled lse [rows] of the forward (natural log)
