@@ -19,7 +19,8 @@ def _geom(r) -> str:
     if "dims" not in r:
         return ""
     x = lambda v: "x".join(map(str, v))  # noqa: E731
-    return f"{x(r['dims'])} w {x(r['window'])} s {x(r['stride'])}, {r.get('heads', '?')} heads, B={r.get('B', '?')}"
+    d = f", d={r['head_dim']}" if "head_dim" in r else ""
+    return f"{x(r['dims'])} w {x(r['window'])} s {x(r['stride'])}, {r.get('heads', '?')} heads, B={r.get('B', '?')}{d}"
 
 
 def main(path: str) -> None:
