@@ -367,6 +367,29 @@ def test_binding_checks_tensor_sizes_before_any_call():
         G.gna_forward(ok_tiled, ok_tiled, ok_tiled, ok_tiled, None, B, heads, dims, (1, 5, 5), (1, 1, 1), d)
 
 
+def test_sizes_beyond_32_bit_tma_coordinates_are_refused_on_host(L):
+    """The largest problem a call accepts: TMA coordinates are 32-bit, so a call
+    whose tiled rows (B * heads * tiles * 128) pass 2^31 returns
+    GNA_ERR_UNSUPPORTED before anything is launched.  20,000 heads of the
+    720p-video latent (900 tiles each) make 2.3e9 rows; the permute kernels
+    refuse more than 2^31 tiles (3,000,000 heads)."""
+    dims, win, st = I3(30, 48, 80), I3(16, 32, 48), I3(1, 1, 1)
+    rows = 20000 * 900 * 128
+    assert rows > 2 ** 31 - 1
+    assert L.gna_forward(FAKE, FAKE, FAKE, FAKE, None, 1, 20000, dims, win, st, 128, G.GNA_BF16, None) == \
+        G.GNA_ERR_UNSUPPORTED
+    assert "2^31" in L.gna_last_error().decode()
+    assert L.gna_backward_delta(FAKE, FAKE, FAKE, 1, 20000, dims, 128, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_UNSUPPORTED
+    assert L.gna_backward_dq(*((FAKE,) * 8), 1, 20000, dims, win, st, 128, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_UNSUPPORTED
+    assert L.gna_backward_dkdv(*((FAKE,) * 8), 1, 20000, dims, win, st, 128, G.GNA_BF16, None, None) == \
+        G.GNA_ERR_UNSUPPORTED
+    assert 900 * 3000000 > 2 ** 31 - 1
+    assert L.gna_permute(FAKE, FAKE, 1, 3000000, dims, 128, G.GNA_BF16, None) == G.GNA_ERR_UNSUPPORTED
+    assert "too large" in L.gna_last_error().decode()
+
+
 def test_backward_rejects_bad_arguments_on_host(L):
     dims, win, st = I3(1, 16, 16), I3(1, 5, 5), I3(1, 1, 1)
     args = (FAKE,) * 8
