@@ -59,8 +59,9 @@ def test_forward_step_replays_from_a_cuda_graph():
         assert torch.equal(got_lse, lse)
 
 
-def test_backward_replays_from_a_cuda_graph():
-    dims, window, stride, B, heads, d = (6, 20, 24), (4, 9, 8), (2, 3, 8), 1, 2, 128
+@pytest.mark.parametrize("d", [64, 128])
+def test_backward_replays_from_a_cuda_graph(d):
+    dims, window, stride, B, heads = (6, 20, 24), (4, 9, 8), (2, 3, 8), 1, 2
     dev = torch.device("cuda")
     shp = G.tiled_shape(B, heads, dims, d)
     t = {}
