@@ -687,7 +687,7 @@ def gpu_arm(a, rank, world, local):
     # optional: the backward pass on the same workload, inputs resident (tiled
     # q, k, v, dout; k in the value layout; the forward's out and lse)
     backward = None
-    if a.backward and a.dtype == "bf16" and d in (64, 128) and not raster and a.tiles == "default":
+    if a.backward and a.dtype == "bf16" and d in (32, 64, 128) and not raster and a.tiles == "default":
         v_tiled = torch.empty(shp, dtype=dt, device=dev)
         k_val = torch.empty_like(vt)
         G.gna_permute(xs[2], v_tiled, B, heads, dims, d, stream=stream)

@@ -695,8 +695,8 @@ gna_status backward_common(int B, int heads, const int dims[3], const int window
     if (B < 1 || heads < 1) return fail(GNA_ERR_INVALID_ARG, "B and heads must be >= 1");
     gna_status st = check_geometry(dims, window, stride);
     if (st != GNA_OK) return st;
-    if (dtype != GNA_BF16 || (head_dim != 64 && head_dim != 128))
-        return fail(GNA_ERR_UNSUPPORTED, "the backward pass supports bf16 with head_dim 64 or 128");
+    if (dtype != GNA_BF16 || (head_dim != 32 && head_dim != 64 && head_dim != 128))
+        return fail(GNA_ERR_UNSUPPORTED, "the backward pass supports bf16 with head_dim 32, 64 or 128");
     const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
     if (rule != GNA_LEADER_CENTER && rule != GNA_LEADER_LITERAL)
         return fail(GNA_ERR_INVALID_ARG, "unknown leader rule %d", rule);

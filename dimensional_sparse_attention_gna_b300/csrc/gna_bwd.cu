@@ -61,12 +61,14 @@ constexpr float kBLog2e = 1.4426950408889634f;
 constexpr int kDQSteps = kTileElems / 16;        // K = 16 bf16 per MMA over 128 keys / queries
 constexpr uint32_t kIdesc = make_idesc(128, 128, kFmtBF16, false);
 
-// bf16 tiles of head_dim D (64 or 128): a token row is 2 D bytes, one or two
-// 128-byte swizzle spans
+// bf16 tiles of head_dim D (32, 64 or 128): a token row is 2 D bytes, one 64-byte
+// or one or two 128-byte swizzle spans
 template <int D>
 struct BwdCfg {
     static constexpr int kRowBytes = D * 2;                    // bytes per token row
-    static constexpr int kChunks = kRowBytes / 128;            // 128-byte spans per row (TMA boxes per tile)
+    static constexpr int kSpan = kRowBytes < 128 ? kRowBytes : 128;     // swizzle span of a tiled tile
+    static constexpr uint32_t kSwizzle = kSpan == 128 ? kSwizzle128B : kSwizzle64B;
+    static constexpr int kChunks = kRowBytes / kSpan;          // spans per row (TMA boxes per tile)
     static constexpr int kTileBytes = kTileElems * kRowBytes;  // one 128-token tile (either layout)
     // at least ~116 KB, so that one CTA (which takes all 512 TMEM columns) is
     // resident per SM and a second one never waits in the TMEM allocation
@@ -75,13 +77,13 @@ struct BwdCfg {
     static constexpr int kDQSmemAlloc = (7 * kTileBytes + 1024) > kMinSmem ? (7 * kTileBytes + 1024) : kMinSmem;
     static constexpr int kQKSteps = kRowBytes / 32;            // MMA k-steps over the head dimension
     static constexpr int kHalfWords = kRowBytes / 8;           // TMEM columns of half a Q / dO row
-    static constexpr int kHalfPieces = D / 64;                 // 32-column pieces of half a dQ / dK / dV row
+    static constexpr int kHalfCols = D / 2;                    // TMEM columns of half a dQ / dK / dV row
     static constexpr uint32_t kIdescDQ = make_idesc(128, D, kFmtBF16, false);    // dQ += dS K: N = D
     static constexpr int kKVStageBytes = 2 * kTileBytes + 1024;                  // Q_i, dO_i, lse_i, delta_i
     static constexpr int kKVSmemAlloc = (2 * kTileBytes + kBStages * kKVStageBytes + 1024) > kMinSmem
                                             ? (2 * kTileBytes + kBStages * kKVStageBytes + 1024) : kMinSmem;
     static constexpr uint32_t kIdescMN = make_idesc(128, D, kFmtBF16, true);     // dV, dK: N = D, B MN-major
-    static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+    static_assert(D == 32 || D == 64 || D == 128, "head_dim 32, 64 or 128");
 };
 
 // the dQ kernel's three shared-memory rings (one per operand of a KV tile)
@@ -165,15 +167,17 @@ __device__ __forceinline__ float2 bwd_fmul2(float2 a, float2 b)
     return d;
 }
 
-// N = 16 or 32 consecutive TMEM columns of this warp's lane quarter
+// N = 8, 16 or 32 consecutive TMEM columns of this warp's lane quarter
 template <int N>
 __device__ __forceinline__ void bwd_tmem_st(uint32_t taddr, const uint32_t (&r)[N])
 {
     if constexpr (N == 32) {
         tmem_st32(taddr, r);
-    } else {
-        static_assert(N == 16, "16 or 32 columns");
+    } else if constexpr (N == 16) {
         tmem_st16(taddr, r);
+    } else {
+        static_assert(N == 8, "8, 16 or 32 columns");
+        tmem_st8(taddr, r);
     }
 }
 
@@ -184,6 +188,36 @@ __device__ __forceinline__ void bwd_reg_fence(uint32_t (&r)[N])
     for (int i = 0; i < N; i += 8)
         asm volatile("" : "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), "+r"(r[i + 5]),
                      "+r"(r[i + 6]), "+r"(r[i + 7]));
+}
+
+// N (16 or 32) fp32 TMEM columns of this thread's lane, times mul, to N bf16 at
+// dst (16-byte aligned); zeros when !load
+template <int N>
+__device__ __forceinline__ void bwd_store_cols(uint32_t taddr, bool load, float mul, uint8_t* dst)
+{
+    uint32_t r[N];
+    if (load) {
+        if constexpr (N == 32) {
+            tmem_ld32(taddr, r);
+        } else {
+            static_assert(N == 16, "16 or 32 columns");
+            tmem_ld16(taddr, r);
+        }
+        tmem_wait_ld();
+        bwd_reg_fence(r);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) r[i] = 0u;
+    }
+    uint32_t pk[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+        pk[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < N / 8; ++i) d[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
 }
 
 template <int D>
@@ -266,7 +300,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
             const int32_t row = static_cast<int32_t>(q_tile_global * kTileElems);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c)
-                tma_load_2d(sDO + c * kTileElems * 128, &p.tmDO, bar(bars.do_full), c * 64, row);
+                tma_load_2d(sDO + c * kTileElems * C::kSpan, &p.tmDO, bar(bars.do_full), c * (C::kSpan / 2), row);
         }
         __syncwarp();
         int issued[kRings] = {0, 0, 0};
@@ -297,7 +331,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
                         const int32_t row = static_cast<int32_t>(tile * kTileElems);
 #pragma unroll
                         for (int c = 0; c < C::kChunks; ++c)
-                            tma_load_2d(dst + c * kTileElems * 128, r == kRingK ? &p.tmK : &p.tmV, fb, c * 64, row);
+                            tma_load_2d(dst + c * kTileElems * C::kSpan, r == kRingK ? &p.tmK : &p.tmV, fb, c * (C::kSpan / 2),
+                                        row);
                     }
                 }
                 __syncwarp();
@@ -317,7 +352,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         // ============================================================ MMA issuer
         const uint32_t tDQ = tmem + kColDQ, tS = tmem + kColS, tDP = tmem + kColDP;
         const uint32_t tDS = tmem + kColDS, tQ = tmem + kColQ;
-        const uint64_t dDO = make_smem_desc(sDO, 16, 8 * 128, kSwizzle128B);
+        const uint64_t dDO = make_smem_desc(sDO, 16, 8 * C::kSpan, C::kSwizzle);
         auto wait_slot = [&](int r, int j) -> bool {
             return __all_sync(0xffffffffu, mbar_wait(bar(bars.full[r][j & 1]), (j >> 1) & 1, &abort_flag,
                                                      &g_bwd_status));
@@ -326,12 +361,12 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         auto issue_s = [&](int j) -> bool {
             if (!wait_slot(kRingK, j)) return false;
             tc_fence_after();
-            const uint64_t dK = make_smem_desc(slot_addr(kRingK, j & 1), 16, 8 * 128, kSwizzle128B);
+            const uint64_t dK = make_smem_desc(slot_addr(kRingK, j & 1), 16, 8 * C::kSpan, C::kSwizzle);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
                     // k-step kk: features [16 kk, 16 kk + 16) = 32 bytes of every token row
-                    const int off = ((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128);
+                    const int off = ((kk * 32) / C::kSpan) * (kTileElems * C::kSpan) + ((kk * 32) % C::kSpan);
                     mma_f16_ts(tS, tQ + kk * 8, dK + static_cast<uint64_t>(off >> 4), kIdesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(bars.s_full));
@@ -344,11 +379,11 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         auto issue_dp = [&](int j) -> bool {
             if (!wait_slot(kRingV, j)) return false;
             tc_fence_after();
-            const uint64_t dV = make_smem_desc(slot_addr(kRingV, j & 1), 16, 8 * 128, kSwizzle128B);
+            const uint64_t dV = make_smem_desc(slot_addr(kRingV, j & 1), 16, 8 * C::kSpan, C::kSwizzle);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
-                    const int off = ((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128);
+                    const int off = ((kk * 32) / C::kSpan) * (kTileElems * C::kSpan) + ((kk * 32) % C::kSpan);
                     mma_f16_ss(tDP, dDO + static_cast<uint64_t>(off >> 4), dV + static_cast<uint64_t>(off >> 4),
                                kIdesc, kk > 0 ? 1u : 0u);
                 }
@@ -553,23 +588,12 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
         if (ok) {
             tc_fence_after();
             uint8_t* dst_row = static_cast<uint8_t*>(p.dq) + grow * C::kRowBytes + half * (C::kRowBytes / 2);
+            // this half of the dQ row, in pieces of up to 32 columns
+            constexpr int P = C::kHalfCols < 32 ? C::kHalfCols : 32;
 #pragma unroll
-            for (int pc = 0; pc < C::kHalfPieces; ++pc) {
-                uint32_t r[32];
-                tmem_ld32(tmem + kColDQ + lane_addr + half * (D / 2) + pc * 32, r);
-                tmem_wait_ld();
-                bwd_reg_fence(r);
-                uint32_t pk[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * p.scale,
-                                                             __uint_as_float(r[2 * i + 1]) * p.scale);
-                    pk[i] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                uint4* dst = reinterpret_cast<uint4*>(dst_row + pc * 64);
-#pragma unroll
-                for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-            }
+            for (int pc = 0; pc < C::kHalfCols / P; ++pc)
+                bwd_store_cols<P>(tmem + kColDQ + lane_addr + half * C::kHalfCols + pc * P, true, p.scale,
+                                  dst_row + pc * P * 2);
         }
     }
 
@@ -698,8 +722,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             mbar_arrive_expect_tx(bar(bars.kv_full), 2 * C::kTileBytes);
 #pragma unroll
             for (int c = 0; c < C::kChunks; ++c) {
-                tma_load_2d(sK + c * kTileElems * 128, &p.tmK, bar(bars.kv_full), c * 64, row);
-                tma_load_2d(sV + c * kTileElems * 128, &p.tmV, bar(bars.kv_full), c * 64, row);
+                tma_load_2d(sK + c * kTileElems * C::kSpan, &p.tmK, bar(bars.kv_full), c * (C::kSpan / 2), row);
+                tma_load_2d(sV + c * kTileElems * C::kSpan, &p.tmV, bar(bars.kv_full), c * (C::kSpan / 2), row);
             }
         }
         __syncwarp();
@@ -720,8 +744,9 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
                 mbar_arrive_expect_tx(bar(bars.full[s]), 2 * C::kTileBytes + 2 * kTileElems * 4);
 #pragma unroll
                 for (int c = 0; c < C::kChunks; ++c) {
-                    tma_load_2d(st + c * kTileElems * 128, &p.tmQ, bar(bars.full[s]), c * 64, row);
-                    tma_load_2d(st + C::kTileBytes + c * kTileElems * 128, &p.tmDO, bar(bars.full[s]), c * 64, row);
+                    tma_load_2d(st + c * kTileElems * C::kSpan, &p.tmQ, bar(bars.full[s]), c * (C::kSpan / 2), row);
+                    tma_load_2d(st + C::kTileBytes + c * kTileElems * C::kSpan, &p.tmDO, bar(bars.full[s]),
+                                c * (C::kSpan / 2), row);
                 }
                 bulk_load_g2s(st + 2 * C::kTileBytes, p.lse + qtile * kTileElems, kTileElems * 4, bar(bars.full[s]));
                 bulk_load_g2s(st + 2 * C::kTileBytes + kTileElems * 4, p.delta + qtile * kTileElems, kTileElems * 4,
@@ -740,8 +765,8 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         const uint32_t tDV = tmem + kColDV, tDK = tmem + kColDK, tST = tmem + kColST, tDPT = tmem + kColDPT;
-        const uint64_t dKj = make_smem_desc(sK, 16, 8 * 128, kSwizzle128B);
-        const uint64_t dVj = make_smem_desc(sV, 16, 8 * 128, kSwizzle128B);
+        const uint64_t dKj = make_smem_desc(sK, 16, 8 * C::kSpan, C::kSwizzle);
+        const uint64_t dVj = make_smem_desc(sV, 16, 8 * C::kSpan, C::kSwizzle);
         auto stage_of = [&](int i) { return sStage + (i % kBStages) * C::kKVStageBytes; };
         // S^T(i) = K_j Q_i^T (both operands from shared memory)
         auto issue_s = [&](int i) -> bool {
@@ -749,11 +774,12 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             if (!__all_sync(0xffffffffu, mbar_wait(bar(bars.full[s]), (i / kBStages) & 1, &abort_flag, &g_bwd_status)))
                 return false;
             tc_fence_after();
-            const uint64_t dQk = make_smem_desc(stage_of(i), 16, 8 * 128, kSwizzle128B);   // K-major
+            const uint64_t dQk = make_smem_desc(stage_of(i), 16, 8 * C::kSpan, C::kSwizzle);   // K-major
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>((((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128)) >> 4);
+                    const uint64_t off = static_cast<uint64_t>(
+                        (((kk * 32) / C::kSpan) * (kTileElems * C::kSpan) + ((kk * 32) % C::kSpan)) >> 4);
                     mma_f16_ss(tST, dKj + off, dQk + off, kIdesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(bars.s_full));
@@ -763,11 +789,12 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
         };
         // dP^T(i) = V_j dO_i^T (step i's stage has landed: issue_s(i) waited for it)
         auto issue_dp = [&](int i) {
-            const uint64_t dDOk = make_smem_desc(stage_of(i) + C::kTileBytes, 16, 8 * 128, kSwizzle128B);
+            const uint64_t dDOk = make_smem_desc(stage_of(i) + C::kTileBytes, 16, 8 * C::kSpan, C::kSwizzle);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < C::kQKSteps; ++kk) {
-                    const uint64_t off = static_cast<uint64_t>((((kk * 32) / 128) * (kTileElems * 128) + ((kk * 32) % 128)) >> 4);
+                    const uint64_t off = static_cast<uint64_t>(
+                        (((kk * 32) / C::kSpan) * (kTileElems * C::kSpan) + ((kk * 32) % C::kSpan)) >> 4);
                     mma_f16_ss(tDPT, dVj + off, dDOk + off, kIdesc, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(bar(bars.dp_full));
@@ -800,8 +827,9 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
             }
             tc_fence_after();
             const uint32_t st = stage_of(i);
-            const uint64_t dQm = make_smem_desc(st, kTileElems * 128, 8 * 128, kSwizzle128B);   // MN-major
-            const uint64_t dDOm = make_smem_desc(st + C::kTileBytes, kTileElems * 128, 8 * 128, kSwizzle128B);
+            // MN-major: feature spans kTileElems rows apart, 8-token groups 8 spans apart
+            const uint64_t dQm = make_smem_desc(st, kTileElems * C::kSpan, 8 * C::kSpan, C::kSwizzle);
+            const uint64_t dDOm = make_smem_desc(st + C::kTileBytes, kTileElems * C::kSpan, 8 * C::kSpan, C::kSwizzle);
             if (elect_one_sync()) {
 #pragma unroll
                 for (int kk = 0; kk < kDQSteps; ++kk) {
@@ -809,7 +837,7 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
                     // Query piece c (32 columns) keeps P^T at dP^T columns [32 c, 32 c + 16)
                     // and dS^T at [32 c + 16, 32 c + 32)
                     const uint32_t a = (kk >> 1) * 32 + (kk & 1) * 8;
-                    const uint64_t off = static_cast<uint64_t>((kk * 16 * 128) >> 4);
+                    const uint64_t off = static_cast<uint64_t>((kk * 16 * C::kSpan) >> 4);
                     const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
                     mma_f16_ts(tDV, tDPT + a, dDOm + off, C::kIdescMN, acc);
                     mma_f16_ts(tDK, tDPT + a + 16, dQm + off, C::kIdescMN, acc);
@@ -977,29 +1005,12 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dkdv_kernel(const __grid
                 uint8_t* dst_row = static_cast<uint8_t*>(which == 0 ? p.dv : p.dk) + grow * C::kRowBytes +
                                    half * (C::kRowBytes / 2);
                 const float mul = which == 0 ? 1.0f : p.scale;
+                // no query reaches this key tile when n_q == 0: zeros
+                constexpr int P = C::kHalfCols < 32 ? C::kHalfCols : 32;
 #pragma unroll
-                for (int pc = 0; pc < C::kHalfPieces; ++pc) {
-                    uint32_t r[32];
-                    if (n_q > 0) {
-                        tmem_ld32(tmem + (which == 0 ? kColDV : kColDK) + lane_addr + half * (D / 2) + pc * 32, r);
-                        tmem_wait_ld();
-                        bwd_reg_fence(r);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) r[i] = 0u;     // no query reaches this key tile
-                    }
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * mul,
-                                                                 __uint_as_float(r[2 * i + 1]) * mul);
-                        pk[i] = *reinterpret_cast<uint32_t*>(&h);
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(dst_row + pc * 64);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-                }
+                for (int pc = 0; pc < C::kHalfCols / P; ++pc)
+                    bwd_store_cols<P>(tmem + (which == 0 ? kColDV : kColDK) + lane_addr + half * C::kHalfCols + pc * P,
+                                      n_q > 0, mul, dst_row + pc * P * 2);
             }
         }
     }
@@ -1031,11 +1042,13 @@ __global__ void gna_bwd_delta_kernel(const __nv_bfloat16* __restrict__ out, cons
         const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.x));
         const float2 g1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&g.y));
         acc = o0.x * g0.x + o0.y * g0.y + o1.x * g1.x + o1.y * g1.y;
-    } else {
-        static_assert(D == 64, "head_dim 64 or 128");
+    } else if constexpr (D == 64) {
         const float2 o0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(out + r * D + lane * 2));
         const float2 g0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(dout + r * D + lane * 2));
         acc = o0.x * g0.x + o0.y * g0.y;
+    } else {
+        static_assert(D == 32, "head_dim 32, 64 or 128");
+        acc = __bfloat162float(out[r * D + lane]) * __bfloat162float(dout[r * D + lane]);
     }
 #pragma unroll
     for (int m = 16; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
@@ -1078,6 +1091,7 @@ cudaError_t launch_backward_dq(const BwdParams& p, int head_dim, int64_t num_q_t
     if (num_q_tiles <= 0) return cudaSuccess;
     if (head_dim == 128) return launch_dq<128>(p, num_q_tiles, stream);
     if (head_dim == 64) return launch_dq<64>(p, num_q_tiles, stream);
+    if (head_dim == 32) return launch_dq<32>(p, num_q_tiles, stream);
     return cudaErrorNotSupported;
 }
 
@@ -1086,6 +1100,7 @@ cudaError_t launch_backward_dkdv(const BwdKVParams& p, int head_dim, int64_t num
     if (num_kv_tiles <= 0) return cudaSuccess;
     if (head_dim == 128) return launch_dkdv<128>(p, num_kv_tiles, stream);
     if (head_dim == 64) return launch_dkdv<64>(p, num_kv_tiles, stream);
+    if (head_dim == 32) return launch_dkdv<32>(p, num_kv_tiles, stream);
     return cudaErrorNotSupported;
 }
 
@@ -1101,6 +1116,8 @@ cudaError_t launch_backward_delta(const void* out, const void* dout, float* delt
         gna_bwd_delta_kernel<128><<<dim3(static_cast<unsigned>(blocks)), warps * 32, 0, stream>>>(o, g, delta, rows);
     else if (head_dim == 64)
         gna_bwd_delta_kernel<64><<<dim3(static_cast<unsigned>(blocks)), warps * 32, 0, stream>>>(o, g, delta, rows);
+    else if (head_dim == 32)
+        gna_bwd_delta_kernel<32><<<dim3(static_cast<unsigned>(blocks)), warps * 32, 0, stream>>>(o, g, delta, rows);
     else
         return cudaErrorNotSupported;
     return cudaGetLastError();

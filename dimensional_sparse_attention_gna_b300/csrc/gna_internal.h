@@ -64,7 +64,7 @@ cudaError_t launch_forward(const FwdParams& p, int head_dim, int elem_size, int6
 // Device status word: read-and-clear.
 cudaError_t read_and_clear_status(int* status, cudaStream_t stream);
 
-// Parameters of one dQ launch of the backward pass (bf16, head_dim 64 or 128;
+// Parameters of one dQ launch of the backward pass (bf16, head_dim 32, 64 or 128;
 // all tensors tiled except kv, which is k in the value layout).
 struct BwdParams {
     CUtensorMap tmK;             // 2-D TMA view [rows, head_dim] of the tiled k
@@ -101,7 +101,7 @@ struct BwdKVParams {
 };
 
 // dK / dV over num_kv_tiles CTAs, dQ over num_q_tiles CTAs, and delta =
-// <dout, out> over `rows` tiled rows; head_dim 64 or 128 (else
+// <dout, out> over `rows` tiled rows; head_dim 32, 64 or 128 (else
 // cudaErrorNotSupported).
 cudaError_t launch_backward_dkdv(const BwdKVParams& p, int head_dim, int64_t num_kv_tiles, cudaStream_t stream);
 cudaError_t launch_backward_dq(const BwdParams& p, int head_dim, int64_t num_q_tiles, cudaStream_t stream);

@@ -79,8 +79,8 @@ extern "C" gna_status gna_backward_noalloc(const void* q, const void* k, const v
     const int rule = opt ? opt->leader_rule : GNA_LEADER_CENTER;
     gna_status st = gna_tile_stats(dims, window, stride, opt ? opt->tile : nullptr, rule, nullptr, nullptr, nullptr);
     if (st != GNA_OK) return st;
-    if (dtype != GNA_BF16 || (head_dim != 64 && head_dim != 128))
-        return gna::api_fail(GNA_ERR_UNSUPPORTED, "the backward pass supports bf16 with head_dim 64 or 128");
+    if (dtype != GNA_BF16 || (head_dim != 32 && head_dim != 64 && head_dim != 128))
+        return gna::api_fail(GNA_ERR_UNSUPPORTED, "the backward pass supports bf16 with head_dim 32, 64 or 128");
     if (opt && !(opt->scale >= 0.0f && std::isfinite(opt->scale)))
         return gna::api_fail(GNA_ERR_INVALID_ARG, "scale must be finite and >= 0");
     if (opt && opt->descale) return gna::api_fail(GNA_ERR_INVALID_ARG, "descale is only used with GNA_FP8_E4M3");

@@ -1,7 +1,7 @@
 /*
  * gna.h -- C ABI of the B300 (sm_103a) Generalized Neighborhood Attention
  * library (libgna_b300.so): the forward pass with its layout permutes, a
- * backward pass (bf16, head_dim 64 or 128) and host-side planning.
+ * backward pass (bf16, head_dim 32, 64 or 128) and host-side planning.
  *
  * What the library computes
  * -------------------------
@@ -250,7 +250,7 @@ gna_status gna_forward_raster_all(const void* q, const void* k, const void* v, v
 /* The GNA page asks for GNA in training (§4.2, problem 1; §5) and writes no
  * backward; the backward here is the derivative of the forward for the loss
  * L = sum_i <dout_i, out_i>.  It runs in three calls, all bf16 with head_dim
- * 64 or 128, all tensors in the tiled layout of the forward (same tile):
+ * 32, 64 or 128, all tensors in the tiled layout of the forward (same tile):
  *
  * gna_backward_delta: delta_i = <dout_i, out_i> (fp32), the row term of the
  * softmax Jacobian, from the forward's bf16 out.
@@ -304,7 +304,7 @@ gna_status gna_backward_dq(const void* q, const void* k, const void* k_value, co
  *   q, k, v, dout : tiled bfloat16 (as gna_backward_dq); k_value: k in the
  *                   value layout; out, lse: the forward's tiled out and lse
  *   dq, dk, dv    : tiled bfloat16, written
- *   other arguments as gna_backward_dq; bf16 with head_dim 64 or 128 only
+ *   other arguments as gna_backward_dq; bf16 with head_dim 32, 64 or 128 only
  *
  * Limit: B * heads * tiles * 128 (the tiled rows) must not exceed 2^22 =
  * 4,194,304; larger problems return GNA_ERR_INVALID_ARG before anything is

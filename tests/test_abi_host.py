@@ -395,14 +395,14 @@ def test_backward_rejects_bad_arguments_on_host(L):
     args = (FAKE,) * 8
     assert L.gna_backward_dq(None, *args[1:], 1, 2, dims, win, st, 128, G.GNA_BF16, None, None) == \
         G.GNA_ERR_INVALID_ARG
-    assert L.gna_backward_dq(*args, 1, 2, dims, win, st, 32, G.GNA_BF16, None, None) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_backward_dq(*args, 1, 2, dims, win, st, 16, G.GNA_BF16, None, None) == G.GNA_ERR_UNSUPPORTED
     assert L.gna_backward_dq(*args, 1, 2, dims, win, st, 256, G.GNA_BF16, None, None) == G.GNA_ERR_UNSUPPORTED
     assert L.gna_backward_dq(*args, 1, 2, dims, win, st, 128, G.GNA_FP8_E4M3, None, None) == G.GNA_ERR_UNSUPPORTED
     assert L.gna_backward_dq(*args, 1, 2, dims, I3(1, 17, 5), st, 128, G.GNA_BF16, None, None) == \
         G.GNA_ERR_INVALID_ARG
     assert L.gna_backward_dkdv(None, *args[1:], 1, 2, dims, win, st, 128, G.GNA_BF16, None, None) == \
         G.GNA_ERR_INVALID_ARG
-    assert L.gna_backward_dkdv(*args, 1, 2, dims, win, st, 32, G.GNA_BF16, None, None) == G.GNA_ERR_UNSUPPORTED
+    assert L.gna_backward_dkdv(*args, 1, 2, dims, win, st, 96, G.GNA_BF16, None, None) == G.GNA_ERR_UNSUPPORTED
     assert L.gna_backward_dkdv(*args, 1, 2, dims, win, I3(1, 6, 1), 128, G.GNA_BF16, None, None) == \
         G.GNA_ERR_INVALID_ARG
     assert L.gna_backward_delta(FAKE, FAKE + 8, FAKE, 1, 2, dims, 128, G.GNA_BF16, None, None) == \

@@ -98,7 +98,7 @@ def test_gradients_small_grids_all_elements(B, heads, dims, window, stride, tile
     (1, 2, (2, 8, 16), (2, 8, 16), (1, 1, 1), None, G.GNA_LEADER_CENTER),      # window = grid
 ])
 def test_gradients_head_dim_64_small_grids_all_elements(B, heads, dims, window, stride, tile, rule):
-    """head_dim 64: one 128-byte span per token row, dQ / dK / dV accumulators of 64 columns."""
+    """head_dim 64: one 128-byte swizzle span per token row, dQ / dK / dV accumulators of 64 columns."""
     _check_grads(8300 + sum(dims), B, heads, dims, window, stride, tile=tile, rule=rule, d=64)
 
 
@@ -109,6 +109,21 @@ def test_gradients_mid_size_video_grid():
 
 def test_gradients_head_dim_64_mid_size_video_grid():
     _check_grads(8400, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1), d=64)
+
+
+@pytest.mark.parametrize("B,heads,dims,window,stride,tile,rule", [
+    (1, 2, (1, 16, 16), (1, 5, 5), (1, 1, 1), None, G.GNA_LEADER_CENTER),     # the tiny 2-D case at head_dim 32
+    (2, 2, (5, 19, 23), (3, 9, 11), (1, 2, 3), None, G.GNA_LEADER_CENTER),     # ragged
+    (1, 2, (6, 20, 24), (4, 8, 8), (2, 4, 4), None, G.GNA_LEADER_LITERAL),
+    (1, 3, (3, 17, 40), (3, 7, 13), (1, 2, 5), (1, 8, 16), G.GNA_LEADER_CENTER),
+])
+def test_gradients_head_dim_32_small_grids_all_elements(B, heads, dims, window, stride, tile, rule):
+    """head_dim 32: 64-byte token rows (64-byte swizzle), dQ / dK / dV accumulators of 32 columns."""
+    _check_grads(8500 + sum(dims), B, heads, dims, window, stride, tile=tile, rule=rule, d=32)
+
+
+def test_gradients_head_dim_32_mid_size_video_grid():
+    _check_grads(8600, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1), d=32)
 
 
 def test_gradients_repeat_runs_bit_identical():
