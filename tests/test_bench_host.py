@@ -81,6 +81,11 @@ def test_reference_arm_prints_one_contract_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    # the same config object as the GPU arm builds for these arguments (both call run_config)
+    sys.path.insert(0, ROOT)
+    import bench
+    a = bench.parse_args(["--dims", "4,16,16", "--window", "2,5,5", "--heads", "2", "--head-dim", "32"])
+    assert line["config"] == bench.run_config(a, 1)
 
 
 def test_traffic_record_applies_only_to_the_captured_workload():
