@@ -19,17 +19,18 @@
 //               its own, so a slot is refilled as soon as its one product is done
 //   warp 1      TMEM allocator and tcgen05.mma issuer
 //   warps 2..9  dS: thread = (query row, half of the 128 key columns)
-// TMEM (512 columns): dQ [0, 128), S [128, 256), dP [256, 384), dS [384, 448),
-// Q [448, 512).  Per KV tile: S = Q K^T (A from TMEM), dP = dO V^T (both
-// operands from shared memory), then dQ += dS K with dS (bf16) in TMEM as the
-// A operand and K in the value layout as the K-major B operand (as V is for
-// P V in the forward).  S, dP and dS each have columns of their own: the dS
-// warps hand S and dP back as soon as they hold them in registers, so S and
-// dP of the next KV tile are computed while they form dS, and only the store
-// of dS waits for the previous dQ product.  No TMEM reuse depends on the
-// order in which the tensor core executes products: every reuse waits on a
-// barrier.  The element mask of a partial tile is one 32-bit word per 32 key
-// columns (box_mask_word).
+// TMEM (512 columns): dQ [0, d), S [128, 256), dP [256, 384), dS [384, 448),
+// Q [448, 448 + d / 2) for head_dim d.  Per KV tile: S = Q K^T (A from TMEM),
+// dP = dO V^T (both operands from shared memory), then dQ += dS K with dS
+// (bf16) in TMEM as the A operand and K in the value layout as the K-major B
+// operand (as V is for P V in the forward).  S, dP and dS each have columns of
+// their own: the dS warps hand S back as soon as they hold it in registers and
+// form p (bf16) from it while dP is computed, then hand dP back once read, so
+// S and dP of the next KV tile are computed while they form dS; only the store
+// of dS waits for the previous dQ product.  No TMEM reuse depends on the order
+// in which the tensor core executes products: every reuse waits on a barrier.
+// The element mask of a partial tile is one 32-bit word per 32 key columns
+// (box_mask_word).
 //
 // Every mbarrier wait is bounded; a role that gives up raises the abort flag
 // and the device status word, and the CTA drains and exits.
@@ -615,10 +616,11 @@ __global__ void __launch_bounds__(kBThreads, 1) gna_bwd_dq_kernel(const __grid_c
 //   S^T  = K_j Q_i^T,  dP^T = V_j dO_i^T            (A, B from shared memory)
 //   P^T  = exp(S^T - lse_i),  dS^T = P^T (dP^T - delta_i)   (per key row)
 //   dV_j += P^T dO_i,  dK_j += dS^T Q_i               (A from TMEM, B MN-major)
-// TMEM: dV [0, 128), dK [128, 256), S^T [256, 384), dP^T [384, 512); P^T and
-// dS^T of each 32-query piece go over that piece's own dP^T columns (16 + 16),
-// so S^T is free once it is in registers and S^T of the next Q tile is
-// computed while the key-row warps work.  Q_i and dO_i are read as tiled tiles
+// TMEM: dV [0, d), dK [128, 128 + d), S^T [256, 384), dP^T [384, 512) for
+// head_dim d; P^T and dS^T of each 32-query piece go over that piece's own
+// dP^T columns (16 + 16), so S^T is free once it is in registers and S^T of
+// the next Q tile is computed while the key-row warps work; they form P^T
+// from S^T while dP^T is computed.  Q_i and dO_i are read as tiled tiles
 // in both roles: K-major for S^T and dP^T, MN-major (token rows, 16 per
 // k-step) for dV and dK.  The element mask comes from, per dimension, the
 // interval of query positions whose window holds this thread's key (one
