@@ -26,19 +26,27 @@ class _GNAFunction(torch.autograd.Function):
         shp = G.tiled_shape(B, heads, dims, d)
         vshp = G.value_shape(B, heads, dims, d)
         bf = torch.bfloat16
-        qt, kt, vt = (torch.empty(shp, dtype=bf, device=q.device) for _ in range(3))
-        k_value, v_value = (torch.empty(vshp, dtype=bf, device=q.device) for _ in range(2))
-        for src, dst in ((q, qt), (k, kt), (v, vt)):
+        # the backward also needs v tiled and k in the value layout
+        train = any(ctx.needs_input_grad[:3])
+        qt, kt = (torch.empty(shp, dtype=bf, device=q.device) for _ in range(2))
+        v_value = torch.empty(vshp, dtype=bf, device=q.device)
+        for src, dst in ((q, qt), (k, kt)):
             G.gna_permute(src, dst, B, heads, dims, d)
-        G.gna_permute_v(k, k_value, B, heads, dims, d)
         G.gna_permute_v(v, v_value, B, heads, dims, d)
+        vt = k_value = None
+        if train:
+            vt = torch.empty(shp, dtype=bf, device=q.device)
+            k_value = torch.empty(vshp, dtype=bf, device=q.device)
+            G.gna_permute(v, vt, B, heads, dims, d)
+            G.gna_permute_v(k, k_value, B, heads, dims, d)
         out_t = torch.empty(shp, dtype=bf, device=q.device)
         lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=q.device)
         G.gna_forward(qt, kt, v_value, out_t, lse_t, B, heads, dims, window, stride, d, leader_rule=leader_rule,
                       scale=scale)
         out = torch.empty_like(q)
         G.gna_unpermute(out_t, out, B, heads, dims, d)
-        ctx.save_for_backward(qt, kt, k_value, vt, out_t, lse_t)
+        if train:
+            ctx.save_for_backward(qt, kt, k_value, vt, out_t, lse_t)
         ctx.geom = (B, heads, dims, d, tuple(window), tuple(stride), leader_rule, scale)
         return out
 

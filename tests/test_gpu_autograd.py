@@ -49,6 +49,20 @@ def test_gna_attention_forward_and_gradients_match_the_oracle(d, dims, window, s
         np.testing.assert_array_equal(t.grad.float().cpu().numpy(), w)
 
 
+def test_gna_attention_without_gradients_gives_the_same_output():
+    """Inputs that need no gradient skip the backward's extra layouts; the
+    forward's output is the same bytes."""
+    B, heads, dims, d, window, stride = 1, 2, (4, 16, 20), 64, (3, 7, 9), (1, 2, 3)
+    dev = torch.device("cuda")
+    q, k, v = (to_bf16(normal_raster(9950 + i, B, dims, heads, d)).to(dev) for i in range(3))
+    with torch.no_grad():
+        a = gna_attention(q, k, v, window, stride)
+    b = gna_attention(q.clone().requires_grad_(), k, v, window, stride)
+    G.gna_get_status()
+    assert not a.requires_grad and b.requires_grad
+    assert torch.equal(a.view(torch.int16), b.detach().view(torch.int16))
+
+
 def test_gna_attention_refuses_bad_inputs():
     x = torch.zeros((1, 1, 16, 16, 2, 32), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(ValueError, match="bfloat16"):
