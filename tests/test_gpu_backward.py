@@ -21,7 +21,7 @@ from tests.gpu_helpers import MAX_ERR_GRAD, REL_RMS_GRAD, record_parity, sample_
 pytestmark = pytest.mark.gpu
 
 
-def gpu_backward(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER):
+def gpu_backward(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER, scale=0.0):
     """(dq, dk, dv) raster float32 and the tiled bf16 results, through the C ABI."""
     B, T, H, W, heads, d = q.shape
     dev = torch.device("cuda")
@@ -38,15 +38,15 @@ def gpu_backward(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEAD
     out_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
     lse_t = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     G.gna_forward(tiled["q"], tiled["k"], v_val, out_t, lse_t, B, heads, dims, window, stride, d, tile=tile,
-                  leader_rule=rule)
+                  leader_rule=rule, scale=scale)
     delta = torch.empty(shp[:-1], dtype=torch.float32, device=dev)
     G.gna_backward_delta(out_t, tiled["dout"], delta, B, heads, dims, d, tile=tile)
     dq_t = torch.empty(shp, dtype=torch.bfloat16, device=dev)
     G.gna_backward_dq(tiled["q"], tiled["k"], k_val, tiled["v"], tiled["dout"], lse_t, delta, dq_t, B, heads, dims,
-                      window, stride, d, tile=tile, leader_rule=rule)
+                      window, stride, d, tile=tile, leader_rule=rule, scale=scale)
     dk_t, dv_t = (torch.empty(shp, dtype=torch.bfloat16, device=dev) for _ in range(2))
     G.gna_backward_dkdv(tiled["q"], tiled["k"], tiled["v"], tiled["dout"], lse_t, delta, dk_t, dv_t, B, heads, dims,
-                        window, stride, d, tile=tile, leader_rule=rule)
+                        window, stride, d, tile=tile, leader_rule=rule, scale=scale)
     res = []
     for t in (dq_t, dk_t, dv_t):
         r = torch.empty((B,) + tuple(dims) + (heads, d), dtype=torch.bfloat16, device=dev)
@@ -57,12 +57,12 @@ def gpu_backward(q, k, v, dout, dims, window, stride, tile=None, rule=G.GNA_LEAD
     return [r.float().cpu().numpy() for r in res], (dq_t, dk_t, dv_t)
 
 
-def _check_grads(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER, d=128):
+def _check_grads(seed, B, heads, dims, window, stride, tile=None, rule=G.GNA_LEADER_CENTER, d=128, scale=None):
     q, k, v, dout = (to_bf16(normal_raster(seed + i, B, dims, heads, d)) for i in range(4))
-    got, _ = gpu_backward(q, k, v, dout, dims, window, stride, tile=tile, rule=rule)
+    got, _ = gpu_backward(q, k, v, dout, dims, window, stride, tile=tile, rule=rule, scale=scale or 0.0)
     orule = oracle.LEADER_CENTER if rule == G.GNA_LEADER_CENTER else oracle.LEADER_LITERAL
     refs = oracle.backward_c(exact_f32(q), exact_f32(k), exact_f32(v), exact_f32(dout), dims, window, stride,
-                             rule=orule)
+                             scale=scale, rule=orule)
     for name, g, r in zip(("dq", "dk", "dv"), got, refs):
         err = np.abs(g.astype(np.float64) - r)
         rel = float(np.sqrt((err ** 2).mean() / (r ** 2).mean()))
@@ -105,6 +105,13 @@ def test_gradients_head_dim_64_small_grids_all_elements(B, heads, dims, window, 
 def test_gradients_mid_size_video_grid():
     """Several KV tiles per dimension and full interior tiles (8x24x40 tokens, 4 heads)."""
     _check_grads(8100, 1, 4, (8, 24, 40), (4, 12, 16), (1, 1, 1))
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_gradients_with_a_custom_softmax_scale(d):
+    """gna_options.scale in place of 1/sqrt(head_dim), in the forward and both
+    backward kernels (0.2 sharpens the softmax at head_dim 64 and flattens it at 128)."""
+    _check_grads(8700 + d, 1, 2, (5, 19, 23), (3, 9, 11), (1, 2, 3), d=d, scale=0.2)
 
 
 def test_gradients_head_dim_64_mid_size_video_grid():
