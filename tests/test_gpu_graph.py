@@ -59,7 +59,7 @@ def test_forward_step_replays_from_a_cuda_graph():
         assert torch.equal(got_lse, lse)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [32, 64, 128])
 def test_backward_replays_from_a_cuda_graph(d):
     dims, window, stride, B, heads = (6, 20, 24), (4, 9, 8), (2, 3, 8), 1, 2
     dev = torch.device("cuda")

@@ -90,6 +90,7 @@ def test_no_alloc_backward_matches_regular_entry_points_twice_in_a_row():
         (9100, 2, 3, (6, 20, 24), (4, 9, 8), (2, 3, 8), 128),   # larger: fills more of the shared array
         (9200, 1, 2, (3, 17, 19), (3, 7, 5), (1, 2, 1), 128),   # smaller, ragged: runs over the first's leftovers
         (9250, 1, 2, (5, 19, 23), (3, 9, 11), (1, 2, 3), 64),   # head_dim 64
+        (9260, 2, 2, (3, 17, 19), (3, 7, 5), (1, 2, 1), 32),    # head_dim 32
     ]
     for seed, B, heads, dims, window, stride, d in problems:
         x = _problem(seed, B, heads, dims, window, stride, d)
