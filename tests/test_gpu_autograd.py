@@ -61,11 +61,3 @@ def test_gna_attention_without_gradients_gives_the_same_output():
     G.gna_get_status()
     assert not a.requires_grad and b.requires_grad
     assert torch.equal(a.view(torch.int16), b.detach().view(torch.int16))
-
-
-def test_gna_attention_refuses_bad_inputs():
-    x = torch.zeros((1, 1, 16, 16, 2, 32), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(ValueError, match="bfloat16"):
-        gna_attention(x.float(), x, x, (1, 5, 5))
-    with pytest.raises(ValueError, match="one shape"):
-        gna_attention(x, x[..., :16], x, (1, 5, 5))
