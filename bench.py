@@ -166,7 +166,7 @@ def measure_host_link(h2d_bytes: int = 2123366400, d2h_bytes: int = 718848000, r
 
 def measure_e4m3_gemm(n: int = 8192, seconds: float = 4.0) -> dict:
     """Dense e4m3 x e4m3 -> bf16 GEMM through torch._scaled_mm (cuBLASLt): the
-    fp8 counterpart of the driver's bf16 cuBLAS figures (2 n^3 flops per GEMM;
+    fp8 counterpart of the measured bf16 cuBLAS figures (2 n^3 flops per GEMM;
     best of 10 as the burst rate, then back to back for `seconds`)."""
     dev = torch.device("cuda")
     a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
