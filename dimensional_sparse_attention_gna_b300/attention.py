@@ -51,6 +51,7 @@ class _GNAFunction(torch.autograd.Function):
         return out
 
     @staticmethod
+    @torch.autograd.function.once_differentiable
     def backward(ctx, dout):
         qt, kt, k_value, vt, out_t, lse_t = ctx.saved_tensors
         B, heads, dims, d, window, stride, rule, scale = ctx.geom
